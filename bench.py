@@ -1,0 +1,436 @@
+"""Benchmark: one decode step of a llama.cpp-style serving engine over a
+quantized KV cache -- quantize-on-append of the new token(s) into the cache,
+then split-K decode attention over the whole packed cache (den_llama.cpp:
+Q4_G64 KV cache, 32K..196K context).
+
+Default workload: 1 sequence, 24 query heads / 4 kv heads, head_dim 256,
+Q4_G64 K and V, 32,767 cached tokens + 1 appended (attention over 32,768),
+fp16 inputs (the "gqa32k" workload of workloads/).  ``--config`` selects
+another workload by index.
+
+Metric: decode-attention KV-read GB/s = packed K+V bytes of all attended
+tokens per step / step time, plus microseconds per generated token.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (fp64 attention over the dequantized
+cache) on the host cores, on the same workload.  Under torchrun each rank runs
+an independent replica (the work is data-parallel across sequences; there is
+no data exchange), the step time is the max over ranks and ``value`` is the
+sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode-attention KV GB/s (fraction of HBM peak) and us/token at 32K/196K ctx"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_kv_cache_q4_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(config_name: str):
+    """DRAM bytes per launch of the attention call from the committed ncu
+    summary, if it was taken on the kernel sources as they are now."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(config_name)
+        if e and e.get("kernel_hash") == _kernel_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_step_time(wl, k_or, v_or, n_threads):
+    """One step of the oracle: quantize-append the new tokens, then fp64
+    attention over the whole cache.  Returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.quantize_append(k_or, wl.k_new, wl.cached_len)
+    oracle.quantize_append(v_or, wl.v_new, wl.cached_len)
+    oracle.decode_attention(k_or, v_or, wl.q, wl.kv_len, wl.spec.scale, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def oracle_caches(wl, append=False):
+    import oracle
+    sp = wl.spec
+    k = oracle.Cache(sp.k_codec, sp.n_seq, sp.n_kv_heads, sp.head_dim, wl.capacity)
+    v = oracle.Cache(sp.v_codec, sp.n_seq, sp.n_kv_heads, sp.head_dim, wl.capacity)
+    for s in range(sp.n_seq):
+        L = int(wl.cached_len[s])
+        for c, src in ((k, wl.k_prefill), (v, wl.v_prefill)):
+            qs, sc = oracle.quantize(c.codec, np.ascontiguousarray(src[s].transpose(1, 0, 2)))
+            c.qs[s, :, :L] = qs
+            c.scales[s, :, :L] = sc
+    return k, v
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, kv_bytes):
+    """The oracle timed on the host cores: each step is the full workload step."""
+    import oracle
+    oracle.build()
+    k, v = oracle_caches(wl)
+    units = wl.spec.n_seq * wl.spec.n_kv_heads
+    threads = max(1, min(cpu_threads(), units))
+    for _ in range(args.warmup):
+        oracle_step_time(wl, k, v, threads)
+    times = [oracle_step_time(wl, k, v, threads) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    val = kv_bytes / t / 1e9
+    sample = f"full {wl.spec.name} step (append + fp64 attention over {int(wl.kv_len.sum())} tokens) x {args.steps}"
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy Gaussian K/V/Q; no dataset or weights)",
+            "config": _config(wl, args),
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _config(wl, args, extra=None):
+    sp = wl.spec
+    c = {"workload": sp.name, "n_seq": sp.n_seq, "n_heads": sp.n_heads, "n_kv_heads": sp.n_kv_heads,
+         "head_dim": sp.head_dim, "kv_len": int(wl.kv_len.max()) if sp.n_seq == 1 else "ragged",
+         "total_kv_tokens": int(wl.kv_len.sum()), "n_q": sp.n_q,
+         "k_codec": "q4_g64" if sp.k_codec == workloads.Q4_G64 else "q8_0",
+         "v_codec": "q4_g64" if sp.v_codec == workloads.Q4_G64 else "q8_0"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_ours(args, wl, kv_bytes, world, rank, local):
+    import torch
+    import quantized_kv_cache_q4_gb300 as kvq
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sp = wl.spec
+    S, Hk, D, H, nq = sp.n_seq, sp.n_kv_heads, sp.head_dim, sp.n_heads, sp.n_q
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # resident cache: prefill through the library's own quantizer
+    k0 = kvq.KVCache(sp.k_codec, S, Hk, D, wl.capacity, device=dev)
+    v0 = kvq.KVCache(sp.v_codec, S, Hk, D, wl.capacity, device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for s in range(S):
+        L = int(wl.cached_len[s])
+        kvq.kvq_quantize_append(k0.seq_view(s), v0.seq_view(s), to_dev(wl.k_prefill[s][None]),
+                                to_dev(wl.v_prefill[s][None]), L, zero)
+    torch.cuda.synchronize()
+    cache_bytes = k0.nbytes() + v0.nbytes()
+    # rotating copies so that every step reads its cache from HBM, not L2
+    n_copies = max(1, min(64, math.ceil(4 * L2_BYTES / max(1, kv_bytes))))
+    caches = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(n_copies - 1)]
+
+    k_new, v_new, q = to_dev(wl.k_new), to_dev(wl.v_new), to_dev(wl.q)
+    pos0, kv_len = to_dev(wl.cached_len), to_dev(wl.kv_len)
+    max_kv = int(wl.kv_len.max())
+    n_splits = args.splits if args.splits is not None else 0
+    n_splits_eff = n_splits or kvq.kvq_decode_default_splits(S, Hk, H, nq, D, max_kv)
+    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(S, Hk, H, nq, D, max_kv, n_splits), dev)
+    out = torch.empty((S, nq, H, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((S, nq, H), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, ev=None):
+        kc, vc = caches[i % n_copies]
+        kvq.kvq_quantize_append(kc, vc, k_new, v_new, nq, pos0, err, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kvq.kvq_decode_attention(kc, vc, q, nq, H, sp.scale, kv_len, max_kv, n_splits, out, lse, ws, d_err=err,
+                                 stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    # one CUDA graph per cache copy: the host is not on the timed path
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(n_copies):      # warm the launch path before capture
+            step(i)
+    stream.synchronize()
+    for i in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device error bits set during set-up"
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_copies].replay()
+    barrier()
+
+    # timed region: exactly K steps
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                graphs[i % n_copies].replay()
+            t_end.record(stream)
+        barrier()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clock_summary = clocks.summary()
+
+    # the attention call alone (its kernels), timed with events on its stream.
+    # A sleep kernel holds the stream while the host enqueues a batch of eager
+    # steps, so host launch time never shows up between the two events.
+    attn_ms = []
+    reps = max(1, min(20, args.steps // n_copies))
+    for rep in range(reps):
+        evs = []
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(4e6))
+            for i in range(n_copies):
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                step(i, e)
+                evs.append(e)
+        stream.synchronize()
+        attn_ms += [a.elapsed_time(b) for a, b in evs]
+    attn = statistics.median(attn_ms)
+
+    # end to end through the public API: new K/V rows and q from pinned host
+    # memory, results back to pinned host memory, one synchronisation a step
+    h_k, h_v, h_q = (torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in (wl.k_new, wl.v_new, wl.q))
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_graphs = []
+    for i in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            q.copy_(h_q, non_blocking=True)
+            step(i)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+        e2e_graphs.append(g)
+    for i in range(args.warmup):
+        e2e_graphs[i % n_copies].replay()
+        stream.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_graphs[i % n_copies].replay()
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = h_k.numel() * h_k.element_size() + h_v.numel() * h_v.element_size() + h_q.numel() * h_q.element_size()
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    assert int(err.item()) == 0, "device error bits set during the run"
+
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (attn * 1e-3) / 1e9
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    # kernels launched per step: append + decode (+ merge when the range is split)
+    launches = args.steps * (2 + (1 if n_splits_eff > 1 else 0))
+    tokens_per_step = sp.n_seq * sp.n_q
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4/int8 codes, fp16 MMA operands, fp32 accumulate",
+        "data": "synthetic (seeded numpy Gaussian K/V/Q; no dataset or weights)",
+        "config": _config(wl, args, {"n_splits": n_splits_eff, "kv_bytes_per_step": kv_bytes,
+                                     "cache_bytes": cache_bytes,
+                                     "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB, "
+                                           f">= 4x the 129 MB L2); steps replayed from CUDA graphs",
+                                     "parallelism": f"replicas x{world}"}),
+        "us_per_token": round(ms * 1e3 / tokens_per_step, 4),
+        "fraction_of_hbm_peak": round(kv_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attention (decode + merge kernels)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": _traffic(sp.name), "attention_us": round(attn * 1e3, 3)},
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
+        "gpu_launches": launches,
+        "clocks": clock_summary,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--splits", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-steps", type=int, default=None, help="oracle steps for the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = _dist_env()
+
+    wl = workloads.make(workloads.spec(args.config))
+    kv_bytes = workloads.kv_bytes_per_token(wl.spec) * int(wl.kv_len.sum())
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, wl, kv_bytes)
+        print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_ours(args, wl, kv_bytes, world, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        k, v = oracle_caches(wl)
+        units = wl.spec.n_seq * wl.spec.n_kv_heads
+        threads = max(1, min(cpu_threads(), units))
+        n, total = 0, 0.0
+        budget = 10.0
+        while total < budget and n < (args.ref_steps or 1000):
+            total += oracle_step_time(wl, k, v, threads)
+            n += 1
+        t = total / n
+        res["cpu_baseline"] = {"value": round(kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"{n} full {wl.spec.name} steps (append + fp64 attention over "
+                                         f"{int(wl.kv_len.sum())} tokens), {total:.1f} s"}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

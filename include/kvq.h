@@ -1,0 +1,182 @@
+/*
+ * kvq.h -- C ABI of the GB300 quantized-KV-cache decode library (libkvq.so).
+ *
+ * The library implements the two stages a llama.cpp-style serving engine runs
+ * per decode step over a quantized KV cache: the KV-cache append stage, which
+ * quantizes the new K/V rows into the cache, and the attention stage, which
+ * reads the packed cache (Llaminar, "Graphs and Compute Stages", names both as
+ * separate compute stages; den_llama.cpp, "What's in the fork", lists the
+ * set-rows/cpy quantize path and the fattn-vec Q4_G64 kernels).
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps device memory; it enqueues kernels on
+ *     `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
+ *     and returns.  Results are ready once the stream has been synchronized.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns KVQ_EINVAL (or KVQ_EUNSUPPORTED / KVQ_EWORKSPACE) and
+ *     launches nothing.  kvq_last_error() then describes the problem.  An
+ *     unsupported combination is an error, never a silent change of method
+ *     (den_llama.cpp, "What this fork is": an FA quant pair that was not
+ *     compiled silently fell back to f16-f16; Llaminar, "GPU Graph Capture":
+ *     an unsupported configuration is an error).
+ *   - Problems that only the device can see (a position or length held in
+ *     device memory that is out of range) are reported by OR-ing a KVQ_ERR_*
+ *     bit into the caller's device word `d_err` (nullable); the affected work
+ *     is skipped, nothing traps.
+ *   - Positions and lengths live in device memory and are advanced by the
+ *     caller (Llaminar, "GPU Graph Capture": token positions and KV counters
+ *     stay device-owned), so every call can be captured in a CUDA graph.
+ *   - The library is stateless apart from cached device attributes and a
+ *     per-thread error string; calls on different streams are independent.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,        /* a null pointer, a bad size or an inconsistent shape */
+    KVQ_EUNSUPPORTED = 2,  /* a valid request this build does not implement */
+    KVQ_EWORKSPACE = 3,    /* workspace missing or smaller than kvq_decode_workspace_bytes() */
+    KVQ_ECUDA = 4          /* a CUDA call or kernel launch failed */
+} kvq_status;
+
+/* Codecs of a cache plane.
+ * KVQ_CODEC_Q4_G64 -- signed INT4 codes with one FP16 scale per 64 values,
+ *   4.25 bits per value (den_llama.cpp, "What this fork is", quantized KV
+ *   cache bullet; "build3 (working engine) -- additions", Q4_G64 row).
+ *   Per group: scale = fp16_rne(absmax / 7) (fp32 quotient, saturated to
+ *   65504), code = clamp(rne(x / (float)scale), -8, 7), code 0 if scale == 0.
+ *   A row of head_dim values is head_dim/2 code bytes (byte j: value 2j in the
+ *   low nibble, value 2j+1 in the high nibble, 4-bit two's complement) plus
+ *   head_dim/64 fp16 scales.
+ * KVQ_CODEC_Q8_0 -- the q8_0-style K codec of the mixed pair "-ctk q8_0 -ctv
+ *   q4_g64" (den_llama.cpp, "Build3 (working engine)"): 32 int8 codes and one
+ *   FP16 scale per group, scale = fp16_rne(absmax / 127), code =
+ *   clamp(rne(x / (float)scale), -127, 127); a row is head_dim code bytes plus
+ *   head_dim/32 fp16 scales (8.5 bits per value).
+ * Dequantized value = (float)scale * code, exact in fp32. */
+typedef enum kvq_codec { KVQ_CODEC_Q4_G64 = 1, KVQ_CODEC_Q8_0 = 2 } kvq_codec;
+
+typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_F16 = 1 } kvq_dtype;
+
+/* Bits OR-ed into the caller's device error word. */
+#define KVQ_ERR_APPEND_POS 1   /* pos0[s] < 0 or pos0[s] + n_new > capacity: sequence s skipped */
+#define KVQ_ERR_KV_LEN 2       /* kv_len[s] < 0 or > max_kv_len: sequence s clamped to [0, max_kv_len] */
+#define KVQ_ERR_TIMEOUT 4      /* a bounded device wait gave up; the outputs of that call are invalid */
+
+/* Cache capacity (tokens per (sequence, kv head) slot) must be a multiple of this. */
+#define KVQ_CAPACITY_ALIGN 64
+
+/* One layer's K (or V) cache: two planes, both in device memory.
+ *   qs     : code bytes, [n_seq][n_kv_heads][capacity][kvq_row_bytes(codec, head_dim)]
+ *   scales : fp16 scales, [n_seq][n_kv_heads][capacity][kvq_scales_per_row(codec, head_dim)]
+ * Both planes are 16-byte aligned.  head_dim is a multiple of 64 in
+ * [64, 512]; capacity is a positive multiple of KVQ_CAPACITY_ALIGN. */
+typedef struct kvq_cache {
+    int32_t codec;          /* kvq_codec */
+    int32_t n_seq;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;
+    void *qs;
+    void *scales;
+} kvq_cache;
+
+/* Bytes of one row of the code plane, or 0 for an unknown codec. */
+int32_t kvq_row_bytes(int32_t codec, int32_t head_dim);
+/* FP16 scales in one row, or 0 for an unknown codec. */
+int32_t kvq_scales_per_row(int32_t codec, int32_t head_dim);
+
+/* Quantize-on-append (the KV-cache append stage).
+ *   k_src, v_src : DEVICE, [n_seq][n_new][n_kv_heads][head_dim], dtype src_dtype
+ *                  (KVQ_F32 or KVQ_F16), 16-byte aligned.
+ *   d_pos0       : DEVICE int32 [n_seq]; token i of sequence s is written at
+ *                  cache position d_pos0[s] + i of every kv head.
+ *   d_err        : DEVICE int32, nullable; KVQ_ERR_APPEND_POS is OR-ed in for a
+ *                  sequence whose positions leave [0, capacity), and that
+ *                  sequence is not written.
+ * Either (k, k_src) or (v, v_src) may be NULL to append to one cache only;
+ * k and v may use different codecs but must agree on n_seq, n_kv_heads and
+ * head_dim.  The packed bytes are identical to the CPU reference rule above,
+ * byte for byte.  Whole rows are written, so appends of different tokens never
+ * share a byte. */
+kvq_status kvq_quantize_append(const kvq_cache *k, const kvq_cache *v,
+                               const void *k_src, const void *v_src, int32_t src_dtype,
+                               int32_t n_new, const int32_t *d_pos0, int32_t *d_err,
+                               void *stream);
+
+/* Split count the library uses for kvq_decode_attention(n_splits = 0) on the
+ * current device: enough (sequence, kv head, split) work items to fill the GPU. */
+int32_t kvq_decode_default_splits(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
+                                  int32_t head_dim, int32_t max_kv_len);
+
+/* Device workspace bytes kvq_decode_attention needs for these arguments
+ * (n_splits as passed to it, 0 = the default).  0 means none is needed. */
+size_t kvq_decode_workspace_bytes(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
+                                  int32_t head_dim, int32_t max_kv_len, int32_t n_splits);
+
+/* Decode / MTP-verify attention over the packed cache (the attention stage).
+ *   k, v          : caches with the same n_seq, n_kv_heads, head_dim, capacity.
+ *                   Supported pairs: (Q4_G64, Q4_G64), (Q8_0, Q4_G64), (Q4_G64, Q8_0),
+ *                   (Q8_0, Q8_0).
+ *   q             : DEVICE, [n_seq][n_q][n_heads][head_dim], dtype q_dtype.
+ *                   Query head h reads kv head h / (n_heads / n_kv_heads).
+ *   softmax_scale : multiplies q.k (e.g. 1/sqrt(head_dim)).
+ *   d_kv_len      : DEVICE int32 [n_seq], keys visible to the LAST query token
+ *                   of each sequence; query token i (0-based) sees the first
+ *                   d_kv_len[s] - n_q + i + 1 cache positions (the n_q new
+ *                   tokens are the last n_q positions and attend causally to
+ *                   each other; den_llama.cpp, "Results": MTP n-max 2).  A row
+ *                   that sees no key gets out = 0 and out_lse = -inf.
+ *   max_kv_len    : host bound on every d_kv_len[s], 1 <= max_kv_len <= capacity.
+ *   n_splits      : the sequence range is cut into n_splits chunks per
+ *                   (sequence, kv head) that run in parallel and are merged by
+ *                   log-sum-exp; 0 = kvq_decode_default_splits(); 1..4096.
+ *   out           : DEVICE fp32 [n_seq][n_q][n_heads][head_dim], softmax-weighted V.
+ *   out_lse       : DEVICE fp32 [n_seq][n_q][n_heads], natural-log sum of
+ *                   exp(scores); nullable.
+ *   workspace     : DEVICE scratch of at least kvq_decode_workspace_bytes(),
+ *                   256-byte aligned; may be NULL when that size is 0.  Its
+ *                   contents need no initialisation and are not kept.
+ *   d_err         : DEVICE int32, nullable (KVQ_ERR_KV_LEN, KVQ_ERR_TIMEOUT).
+ * Arithmetic: codes are exact in fp16, dot products accumulate in fp32 and the
+ * softmax runs in fp32. */
+kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v,
+                                const void *q, int32_t q_dtype, int32_t n_q, int32_t n_heads,
+                                float softmax_scale, const int32_t *d_kv_len, int32_t max_kv_len,
+                                int32_t n_splits, float *out, float *out_lse,
+                                void *workspace, size_t workspace_bytes, int32_t *d_err,
+                                void *stream);
+
+/* Log-sum-exp merge of partial attention results (one per split of the key range).
+ *   part_o   : DEVICE fp32 [n_splits][rows][head_dim], each part normalised over its keys.
+ *   part_lse : DEVICE fp32 [n_splits][rows]; -inf marks an empty part (its part_o is ignored).
+ *   out      : DEVICE fp32 [rows][head_dim] = sum_s w_s part_o[s] / sum_s w_s with
+ *              w_s = exp(part_lse[s] - max_s part_lse[s]); 0 if every part is empty.
+ *   out_lse  : DEVICE fp32 [rows], max + ln(sum_s w_s) (-inf if every part is empty); nullable.
+ * 1 <= n_splits <= 4096, rows >= 0, head_dim a multiple of 4 in [4, 1024]. */
+kvq_status kvq_merge_splits(const float *part_o, const float *part_lse, int32_t n_splits,
+                            int32_t rows, int32_t head_dim, float *out, float *out_lse, void *stream);
+
+/* Dequantize a whole cache to fp32 [n_seq][n_kv_heads][capacity][head_dim] on
+ * the device (scale * code, exact).  For inspection and testing. */
+kvq_status kvq_dequantize(const kvq_cache *c, float *out, void *stream);
+
+/* Static description of a status code. */
+const char *kvq_status_string(int32_t status);
+/* Detail of the last non-OK status returned on the calling thread ("" if none). */
+const char *kvq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -16,7 +16,7 @@ def oracle_caches(wl: workloads.Workload, append=True):
         if L == 0:
             continue
         for cache, src in ((k, wl.k_prefill), (v, wl.v_prefill)):
-            qs, sc = oracle.quantize(cache.codec, np.ascontiguousarray(src[s, :L].transpose(1, 0, 2)))
+            qs, sc = oracle.quantize(cache.codec, np.ascontiguousarray(src[s].transpose(1, 0, 2)))
             cache.qs[s, :, :L] = qs
             cache.scales[s, :, :L] = sc
     if append:

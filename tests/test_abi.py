@@ -1,0 +1,125 @@
+"""The C-ABI library loads, exports every entry point include/kvq.h declares,
+and rejects bad arguments on the host before launching anything (these calls
+never reach a kernel, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_kv_cache_q4_gb300 as kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert "kvq_decode_attention" in names and "kvq_quantize_append" in names and "kvq_merge_splits" in names
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(kvq.EXPORTED)
+
+
+def test_row_sizes():
+    assert kvq.kvq_row_bytes(kvq.KVQ_CODEC_Q4_G64, 256) == 128
+    assert kvq.kvq_scales_per_row(kvq.KVQ_CODEC_Q4_G64, 256) == 4
+    assert kvq.kvq_row_bytes(kvq.KVQ_CODEC_Q8_0, 256) == 256
+    assert kvq.kvq_scales_per_row(kvq.KVQ_CODEC_Q8_0, 256) == 8
+    assert kvq.kvq_row_bytes(99, 256) == 0
+    # 4.25 and 8.5 bits per value
+    for codec, bits in ((kvq.KVQ_CODEC_Q4_G64, 4.25), (kvq.KVQ_CODEC_Q8_0, 8.5)):
+        for d in (64, 128, 256, 512):
+            assert (kvq.kvq_row_bytes(codec, d) + 2 * kvq.kvq_scales_per_row(codec, d)) * 8 == bits * d
+
+
+def _fake_cache(**kw):
+    c = dict(codec=kvq.KVQ_CODEC_Q4_G64, n_seq=1, n_kv_heads=4, head_dim=256, capacity=1024, qs=4096, scales=8192)
+    c.update(kw)
+    return kvq.kvq_cache(c["codec"], c["n_seq"], c["n_kv_heads"], c["head_dim"], c["capacity"], c["qs"], c["scales"])
+
+
+def _append(k, v, ksrc=4096, vsrc=4096, dtype=kvq.KVQ_F16, n_new=1, pos=4096):
+    lib = kvq._lib
+    return lib.kvq_quantize_append(ctypes.byref(k) if k else None, ctypes.byref(v) if v else None,
+                                   ksrc if k else None, vsrc if v else None, dtype, n_new, pos, None, None)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(codec=3), kvq.KVQ_EINVAL), (dict(head_dim=96), kvq.KVQ_EINVAL), (dict(head_dim=1024), kvq.KVQ_EINVAL),
+    (dict(capacity=100), kvq.KVQ_EINVAL), (dict(capacity=0), kvq.KVQ_EINVAL), (dict(n_seq=0), kvq.KVQ_EINVAL),
+    (dict(qs=0), kvq.KVQ_EINVAL), (dict(qs=4097), kvq.KVQ_EINVAL), (dict(scales=8200), kvq.KVQ_EINVAL),
+    (dict(head_dim=192), kvq.KVQ_EUNSUPPORTED)])
+def test_append_rejects_bad_cache(bad, status):
+    assert _append(_fake_cache(**bad), None) == status
+    assert kvq.kvq_last_error()
+
+
+def test_append_rejects_bad_arguments():
+    k, v = _fake_cache(), _fake_cache()
+    assert _append(None, None) == kvq.KVQ_EINVAL
+    assert _append(k, v, dtype=7) == kvq.KVQ_EINVAL
+    assert _append(k, v, n_new=-1) == kvq.KVQ_EINVAL
+    assert _append(k, v, pos=None) == kvq.KVQ_EINVAL
+    assert _append(k, v, ksrc=4100) == kvq.KVQ_EINVAL
+    assert _append(k, _fake_cache(n_kv_heads=2)) == kvq.KVQ_EINVAL
+    assert _append(k, v, n_new=0) == kvq.KVQ_OK          # nothing to do, nothing launched
+
+
+def _decode(k, v, q=4096, q_dtype=kvq.KVQ_F16, n_q=1, n_heads=24, scale=0.0625, kv_len=4096, max_kv_len=512,
+            n_splits=1, out=4096, ws=None, ws_bytes=0):
+    return kvq._lib.kvq_decode_attention(ctypes.byref(k), ctypes.byref(v), q, q_dtype, n_q, n_heads, scale, kv_len,
+                                         max_kv_len, n_splits, out, None, ws, ws_bytes, None, None)
+
+
+def test_decode_rejects_bad_arguments():
+    k, v = _fake_cache(), _fake_cache()
+    assert _decode(k, _fake_cache(capacity=2048)) == kvq.KVQ_EINVAL
+    assert _decode(k, v, q=None) == kvq.KVQ_EINVAL
+    assert _decode(k, v, q_dtype=5) == kvq.KVQ_EINVAL
+    assert _decode(k, v, n_q=0) == kvq.KVQ_EINVAL
+    assert _decode(k, v, n_heads=22) == kvq.KVQ_EINVAL                 # not a multiple of 4 kv heads
+    assert _decode(k, v, scale=float("inf")) == kvq.KVQ_EINVAL
+    assert _decode(k, v, kv_len=None) == kvq.KVQ_EINVAL
+    assert _decode(k, v, max_kv_len=0) == kvq.KVQ_EINVAL
+    assert _decode(k, v, max_kv_len=1025) == kvq.KVQ_EINVAL            # beyond capacity
+    assert _decode(k, v, n_splits=-1) == kvq.KVQ_EINVAL
+    assert _decode(k, v, n_splits=5000) == kvq.KVQ_EINVAL
+    assert _decode(k, v, out=None) == kvq.KVQ_EINVAL
+    assert _decode(k, v, n_splits=8) == kvq.KVQ_EWORKSPACE             # splits need a workspace
+    need = kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 512, 8)
+    assert _decode(k, v, n_splits=8, ws=1 << 20, ws_bytes=need - 1) == kvq.KVQ_EWORKSPACE
+    assert _decode(k, v, n_splits=8, ws=(1 << 20) + 16, ws_bytes=need) == kvq.KVQ_EINVAL   # misaligned
+
+
+def test_workspace_sizes():
+    assert kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 32768, 1) == 0
+    rows = 1 * 1 * 24
+    n = kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 32768, 64)
+    assert n >= 64 * rows * 257 * 4 and n % 256 == 0
+    assert kvq.kvq_decode_workspace_bytes(16, 4, 24, 3, 256, 65539, 16) >= 16 * 16 * 3 * 24 * 257 * 4
+    d = kvq.kvq_decode_default_splits(1, 4, 24, 1, 256, 32768)
+    assert 1 <= d <= 4096
+    assert kvq.kvq_decode_default_splits(1, 4, 24, 1, 256, 100) == 1   # short context: no split
+
+
+def test_merge_rejects_bad_arguments():
+    lib = kvq._lib
+    assert lib.kvq_merge_splits(4096, 4096, 0, 4, 256, 4096, None, None) == kvq.KVQ_EINVAL
+    assert lib.kvq_merge_splits(4096, 4096, 5000, 4, 256, 4096, None, None) == kvq.KVQ_EINVAL
+    assert lib.kvq_merge_splits(4096, 4096, 2, -1, 256, 4096, None, None) == kvq.KVQ_EINVAL
+    assert lib.kvq_merge_splits(4096, 4096, 2, 4, 6, 4096, None, None) == kvq.KVQ_EINVAL
+    assert lib.kvq_merge_splits(None, 4096, 2, 4, 256, 4096, None, None) == kvq.KVQ_EINVAL
+    assert lib.kvq_merge_splits(4096, 4096, 2, 0, 256, 4096, None, None) == kvq.KVQ_OK
+
+
+def test_status_strings():
+    for s in range(5):
+        assert kvq.kvq_status_string(s)
+    assert kvq.kvq_status_string(99) == "unknown status"

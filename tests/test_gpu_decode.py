@@ -1,0 +1,107 @@
+"""Decode / MTP-verify attention on the GPU against the fp64 oracle.
+
+Bar: max |o - o_ref| <= 2e-3 and ||o - o_ref||_2 / ||o_ref||_2 <= 1e-2 over the
+whole output, |lse - lse_ref| <= 1e-3, -inf exactly where the oracle has no key."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_kv_cache_q4_gb300 as kvq
+import workloads
+from gpu_helpers import dev, gpu_caches, run_decode
+from helpers import check_close, oracle_caches
+
+pytestmark = pytest.mark.gpu
+
+
+def _both(wl):
+    k, v = gpu_caches(wl)
+    ko, vo = oracle_caches(wl)
+    return k, v, ko, vo
+
+
+@pytest.mark.parametrize("cfg", range(workloads.N_CONFIGS))
+def test_workload_default_splits(cfg):
+    wl = workloads.make(workloads.spec(cfg))
+    k, v, ko, vo = _both(wl)
+    o, lse, err = run_decode(wl, k, v)
+    assert err == 0
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale, n_threads=oracle.max_threads())
+    check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 255, 257])
+@pytest.mark.parametrize("n_new", [1, 2, 3])
+@pytest.mark.parametrize("G", [1, 6])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_small_sweep(L, n_new, G, D):
+    if L < n_new:
+        pytest.skip("fewer keys than query tokens is covered by test_rows_without_keys")
+    wl = workloads.custom(n_seq=2, n_heads=2 * G, n_kv_heads=2, head_dim=D, cached=(L - n_new, max(0, L // 2 - n_new)),
+                          n_new=n_new, src_dtype="f16", q_dtype="f16", seed=L * 7 + n_new + G + D)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (1, 0, 3):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 7, 64, 256])
+def test_split_counts(n_splits):
+    wl = workloads.custom(n_seq=2, n_heads=12, n_kv_heads=2, head_dim=256, cached=(5000, 1234), n_new=3,
+                          src_dtype="f16", q_dtype="f16", dist="outliers", seed=40)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+    assert err == 0
+    check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0),
+                                   (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0)])
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_codec_pairs(kc, vc, D):
+    wl = workloads.custom(n_seq=2, n_heads=8, n_kv_heads=2, head_dim=D, cached=(700, 333), n_new=1, k_codec=kc,
+                          v_codec=vc, src_dtype="f16", q_dtype="f32", seed=D + kc * 3 + vc)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (1, 5):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        check_close(o, o_ref, lse, lse_ref)
+
+
+def test_rows_without_keys():
+    """kv_len < n_q: the first rows see no key -> out = 0, lse = -inf."""
+    wl = workloads.custom(n_seq=2, n_heads=6, n_kv_heads=1, head_dim=128, cached=(0, 10), n_new=3, src_dtype="f16",
+                          q_dtype="f16", seed=50)
+    k, v, ko, vo = _both(wl)
+    kv_len = wl.kv_len.copy()
+    kv_len[0] = 1                       # rows 0, 1 of sequence 0 see nothing
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, kv_len, wl.spec.scale)
+    for n_splits in (1, 4):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits, kv_len=kv_len)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+        assert np.all(o[0, :2] == 0) and np.all(np.isneginf(lse[0, :2]))
+
+
+def test_kv_len_beyond_bound_is_flagged():
+    wl = workloads.custom(n_seq=1, n_heads=2, n_kv_heads=1, head_dim=64, cached=(100,), n_new=1, seed=51)
+    k, v, ko, vo = _both(wl)
+    o, lse, err = run_decode(wl, k, v, kv_len=np.array([101], np.int32), max_kv_len=64)
+    assert err & kvq.KVQ_ERR_KV_LEN
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, np.array([64], np.int32), wl.spec.scale)
+    check_close(o, o_ref, lse, lse_ref)          # clamped to max_kv_len
+
+
+def test_equal_scores_mean_of_v_on_gpu():
+    wl = workloads.custom(n_seq=1, n_heads=6, n_kv_heads=1, head_dim=256, cached=(4095,), n_new=1, src_dtype="f16",
+                          q_dtype="f16", seed=52)
+    k, v, ko, vo = _both(wl)
+    q0 = np.zeros_like(wl.q)
+    o, lse, _ = run_decode(wl, k, v, q=q0)
+    Vh = oracle.dequantize(vo.codec, vo.qs[0, 0, :4096], vo.scales[0, 0, :4096], 256).astype(np.float64)
+    assert np.abs(o[0, 0] - Vh.mean(axis=0)[None]).max() < 1e-4
+    assert np.abs(lse - np.log(4096)).max() < 1e-4

@@ -116,7 +116,7 @@ def test_dominant_key_returns_its_value_row():
     wl = _wl(n_seq=1, H=1, Hk=1, D=128, cached=(63,), seed=5)
     j = 17
     qv = wl.q[0, 0, 0].astype(np.float64)
-    wl.k_prefill[0, j, 0] = (40.0 * qv / np.linalg.norm(qv)).astype(np.float32) * math.sqrt(128) / 4
+    wl.k_prefill[0][j, 0] = (40.0 * qv / np.linalg.norm(qv)).astype(np.float32) * math.sqrt(128) / 4
     k, v = oracle_caches(wl)
     o, _ = oracle.decode_attention(k, v, wl.q, wl.kv_len, wl.spec.scale)
     Vh = dequant_cache(v)[0, 0].astype(np.float64)

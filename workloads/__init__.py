@@ -94,8 +94,8 @@ class Workload:
     cached_len: np.ndarray   # int32 [S]: tokens already in the cache (= append position)
     kv_len: np.ndarray       # int32 [S]: keys visible to the last query token
     capacity: int
-    k_prefill: np.ndarray    # [S][Lmax][Hkv][D] (rows past cached_len[s] unused)
-    v_prefill: np.ndarray
+    k_prefill: list          # per sequence s: [cached_len[s]][Hkv][D]
+    v_prefill: list
     k_new: np.ndarray        # [S][n_new][Hkv][D]
     v_new: np.ndarray
     q: np.ndarray            # [S][n_q][Hq][D]
@@ -138,7 +138,6 @@ def make(sp: Spec, cached=None) -> Workload:
     kv_len = cached + sp.n_new
     capacity = int(-(-int(kv_len.max()) // TOKEN_ALIGN) * TOKEN_ALIGN)
     S, Hk, D, H = sp.n_seq, sp.n_kv_heads, sp.head_dim, sp.n_heads
-    lmax = int(cached.max())
     dt = _np_dtype(sp.src_dtype)
     kb = vb = None
     if sp.dist == "bias":
@@ -147,18 +146,21 @@ def make(sp: Spec, cached=None) -> Workload:
     k_rng = np.random.Generator(np.random.PCG64(k_ss))
     v_rng = np.random.Generator(np.random.PCG64(v_ss))
     m_rng = np.random.Generator(np.random.PCG64(m_ss))
-    k_all = _draw_values(k_rng, m_rng, (S, lmax + sp.n_new, Hk, D), sp.dist, kb, dt)
-    v_all = _draw_values(v_rng, m_rng, (S, lmax + sp.n_new, Hk, D), sp.dist, vb, dt)
+    k_pre, v_pre = [], []
     k_new = np.empty((S, sp.n_new, Hk, D), dt)
     v_new = np.empty((S, sp.n_new, Hk, D), dt)
-    for s in range(S):          # the new tokens follow each sequence's cached ones
+    for s in range(S):          # each sequence: its cached tokens, then the new ones
         c = int(cached[s])
-        k_new[s] = k_all[s, c:c + sp.n_new]
-        v_new[s] = v_all[s, c:c + sp.n_new]
+        ka = _draw_values(k_rng, m_rng, (c + sp.n_new, Hk, D), sp.dist, kb, dt)
+        va = _draw_values(v_rng, m_rng, (c + sp.n_new, Hk, D), sp.dist, vb, dt)
+        k_pre.append(ka[:c])
+        v_pre.append(va[:c])
+        k_new[s] = ka[c:]
+        v_new[s] = va[c:]
     q = np.random.Generator(np.random.PCG64(q_ss)).standard_normal((S, sp.n_q, H, D), dtype=np.float32)
     q = q.astype(_np_dtype(sp.q_dtype))
     return Workload(sp, cached.astype(np.int32), kv_len.astype(np.int32), capacity,
-                    k_all[:, :lmax], v_all[:, :lmax], k_new, v_new, q)
+                    k_pre, v_pre, k_new, v_new, q)
 
 
 def custom(name="custom", n_seq=1, n_heads=1, n_kv_heads=1, head_dim=128, cached=(64,), n_new=1,
@@ -187,3 +189,18 @@ def rand_partials(n_splits: int, rows: int, head_dim: int, seed: int = 3, empty_
     lse[empty] = -np.inf
     o[empty] = 0.0
     return o, lse
+
+
+def wide_range_rows(n_rows: int, head_dim: int, seed: int = 0, dtype=np.float32) -> np.ndarray:
+    """Rows whose 32-value blocks span magnitudes 1e-9..3e4 (fp16-subnormal and
+    saturating scales included), for codec edge cases."""
+    rng = np.random.Generator(np.random.PCG64(BASE_SEED + 7000 + seed))
+    nb = head_dim // 32
+    mag = np.exp(rng.uniform(np.log(1e-9), np.log(3e4), size=(n_rows, nb, 1)))
+    x = rng.standard_normal((n_rows, nb, 32)) * mag
+    heavy = rng.random((n_rows, nb)) < 0.2
+    x[heavy] *= np.exp(rng.standard_normal((int(heavy.sum()), 32)) * 2)
+    x = x.reshape(n_rows, head_dim)
+    if dtype == np.float16:
+        x = np.clip(x, -60000, 60000)
+    return x.astype(dtype)
