@@ -15,6 +15,7 @@ rational brute force, invariants).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -45,29 +46,59 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _declare(lib):
+    P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_f16.restype = ctypes.c_uint16
+    lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.orc_f16_to_f32.restype = ctypes.c_float
+    lib.orc_f32_to_f16_array.argtypes = [P, I64, P]
+    lib.orc_f16_to_f32_array.argtypes = [P, I64, P]
+    lib.orc_quantize.argtypes = [I, P, I64, I, P, P]
+    lib.orc_dequantize.argtypes = [I, P, P, I64, I, P]
+    lib.orc_quantize_append.argtypes = [I, P, I, I, I, I, I, P, P, P]
+    lib.orc_quantize_append.restype = I
+    lib.orc_decode_attention.argtypes = [I, P, P, I, P, P, I, I, I, I, P, I, I, P, D, P, P, I]
+    lib.orc_decode_attention_split.argtypes = [I, P, P, I, P, P, I, I, I, I, P, I, I, P, D, I, P, P]
+    lib.orc_merge_splits.argtypes = [P, P, I, I64, I, P, P]
+    lib.orc_omp_max_threads.restype = I
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
-        lib.orc_f32_to_f16.restype = ctypes.c_uint16
-        lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
-        lib.orc_f16_to_f32.restype = ctypes.c_float
-        lib.orc_f32_to_f16_array.argtypes = [P, I64, P]
-        lib.orc_f16_to_f32_array.argtypes = [P, I64, P]
-        lib.orc_quantize.argtypes = [I, P, I64, I, P, P]
-        lib.orc_dequantize.argtypes = [I, P, P, I64, I, P]
-        lib.orc_quantize_append.argtypes = [I, P, I, I, I, I, I, P, P, P]
-        lib.orc_quantize_append.restype = I
-        lib.orc_decode_attention.argtypes = [I, P, P, I, P, P, I, I, I, I, P, I, I, P, D, P, P, I]
-        lib.orc_decode_attention_split.argtypes = [I, P, P, I, P, P, I, I, I, I, P, I, I, P, D, I, P, P]
-        lib.orc_merge_splits.argtypes = [P, P, I, I64, I, P, P]
-        lib.orc_omp_max_threads.restype = I
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+        return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Test hook: route every function of this module through another build of
+    the oracle source (the planted-mistake tests compile mutants with it)."""
+    global _lib
+    old = _load()
+    _lib = _declare(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = old
+
+
+def compile_source(src_text: str, out_path: str) -> str:
+    """Compile C source text with the oracle's flags into a shared library."""
+    c_path = out_path + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                    "-fno-fast-math", "-o", out_path, c_path, "-lm"], check=True)
+    return out_path
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _ptr(a: np.ndarray) -> int:
