@@ -99,14 +99,12 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.2)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -136,6 +134,22 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank moves bytes_per_rank per step; the job's
+    step time is the slowest rank's."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
 def oracle_step_time(wl, k_or, v_or, n_threads):
@@ -281,9 +295,19 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
             graphs[i % n_copies].replay()
     barrier()
 
-    # timed region: exactly K steps
+    # timed region: exactly K steps.  The clock sampler runs from a ~1 s soak of
+    # the same replays (part of the warm-up) through the timed region, so the
+    # samples are taken under this load with the clocks it settles at.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        t_soak = time.perf_counter()
+        with torch.cuda.stream(stream):
+            i = 0
+            while time.perf_counter() - t_soak < args.soak:
+                for _ in range(64):
+                    graphs[i % n_copies].replay()
+                    i += 1
+                stream.synchronize()
         barrier()
         with torch.cuda.stream(stream):
             t_start.record(stream)
@@ -291,11 +315,7 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
                 graphs[i % n_copies].replay()
             t_end.record(stream)
         barrier()
-    ms = t_start.elapsed_time(t_end) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dist, dev)
     clock_summary = clocks.summary()
 
     # the attention call alone (its kernels), timed with events on its stream.
@@ -339,18 +359,14 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
     for i in range(args.steps):
         e2e_graphs[i % n_copies].replay()
         stream.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / args.steps, dist, dev)
     h2d = h_k.numel() * h_k.element_size() + h_v.numel() * h_v.element_size() + h_q.numel() * h_q.element_size()
     d2h = h_out.numel() * 4 + h_lse.numel() * 4
     assert int(err.item()) == 0, "device error bits set during the run"
 
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (attn * 1e-3) / 1e9
-    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    value = job_gbs(kv_bytes, ms, world)
     # kernels launched per step: append + decode (+ merge when the range is split)
     launches = args.steps * (2 + (1 if n_splits_eff > 1 else 0))
     tokens_per_step = sp.n_seq * sp.n_q
@@ -370,7 +386,7 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": _traffic(sp.name), "attention_us": round(attn * 1e3, 3)},
-        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
         "gpu_launches": launches,
         "clocks": clock_summary,
@@ -387,6 +403,7 @@ def main():
     ap.add_argument("--splits", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-steps", type=int, default=None, help="oracle steps for the cpu_baseline leg")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed replays before the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
