@@ -373,13 +373,15 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4/int8 codes, fp16 MMA operands, fp32 accumulate",
+        "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded numpy Gaussian K/V/Q; no dataset or weights)",
         "config": _config(wl, args, {"n_splits": n_splits_eff, "kv_bytes_per_step": kv_bytes,
                                      "cache_bytes": cache_bytes,
                                      "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB, "
                                            f">= 4x the 129 MB L2); steps replayed from CUDA graphs",
-                                     "parallelism": f"replicas x{world}"}),
+                                     "parallelism": f"replicas x{world}",
+                                     "arithmetic": "int4/int8 codes as exact fp16 MMA operands, fp32 accumulate, "
+                                                   "fp32 softmax"}),
         "us_per_token": round(ms * 1e3 / tokens_per_step, 4),
         "fraction_of_hbm_peak": round(kv_bytes / (ms * 1e-3) / 1e9 / peak, 4),
         "roofline": {"bound": "hbm", "kernel": "kvq_decode_attention (decode + merge kernels)",

@@ -232,7 +232,11 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const vo
                                                align256((size_t)s * rows * k->head_dim * sizeof(float)));
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if ((st = cuda_status(kvq::launch_decode_simt(a, q_dtype, cs), "decode launch")) != KVQ_OK) return st;
+    cudaError_t le;
+    if (kvq::decode_mma_supported(a)) le = kvq::launch_decode_mma(a, q_dtype, cs);
+    else if (kvq::decode_wide_supported(a)) le = kvq::launch_decode_wide(a, q_dtype, cs);
+    else le = kvq::launch_decode_simt(a, q_dtype, cs);
+    if ((st = cuda_status(le, "decode launch")) != KVQ_OK) return st;
     if (s > 1)
         return cuda_status(kvq::launch_merge(a.part_o, a.part_lse, s, (int)rows, k->head_dim, out, out_lse, cs),
                            "merge launch");

@@ -99,6 +99,8 @@ template <int VPL, typename SrcT>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
 {
     const int lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int64_t per_plane = (int64_t)a.n_seq * a.n_new * a.n_kv_heads;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (row >= per_plane * a.n_planes) return;
@@ -160,9 +162,8 @@ cudaError_t launch_append_vpl(const AppendArgs &a, bool f16, cudaStream_t st)
     const int warps = 8;
     const int64_t blocks = ceil_div(rows, warps);
     if (blocks == 0) return cudaSuccess;
-    if (f16) append_kernel<VPL, __half><<<(unsigned)blocks, warps * 32, 0, st>>>(a);
-    else append_kernel<VPL, float><<<(unsigned)blocks, warps * 32, 0, st>>>(a);
-    return cudaGetLastError();
+    if (f16) return launch_pdl(append_kernel<VPL, __half>, dim3((unsigned)blocks), dim3(warps * 32), 0, st, a);
+    return launch_pdl(append_kernel<VPL, float>, dim3((unsigned)blocks), dim3(warps * 32), 0, st, a);
 }
 
 }  // namespace

@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.n_heads / a.n_kv_heads;
     const int R = a.n_q * G;
+    pdl_wait();
+    pdl_trigger();
 
     int len = a.kv_len[s];
     if (len < 0 || len > a.max_kv_len) {
@@ -244,9 +246,8 @@ template <int KC, int VC, int VPL>
 cudaError_t launch3(const DecodeArgs &a, int q_dtype, cudaStream_t st)
 {
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
-    if (q_dtype == KVQ_F16) decode_simt_kernel<KC, VC, VPL, __half><<<grid, kSimtWarps * 32, 0, st>>>(a);
-    else decode_simt_kernel<KC, VC, VPL, float><<<grid, kSimtWarps * 32, 0, st>>>(a);
-    return cudaGetLastError();
+    if (q_dtype == KVQ_F16) return launch_pdl(decode_simt_kernel<KC, VC, VPL, __half>, grid, dim3(kSimtWarps * 32), 0, st, a);
+    return launch_pdl(decode_simt_kernel<KC, VC, VPL, float>, grid, dim3(kSimtWarps * 32), 0, st, a);
 }
 
 template <int KC, int VC>

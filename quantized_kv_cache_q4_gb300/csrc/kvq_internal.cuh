@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvq.h"
 
 namespace kvq {
@@ -18,6 +20,31 @@ __host__ __device__ constexpr int group_size(int codec) { return codec == KVQ_CO
 __host__ __device__ constexpr int row_bytes(int codec, int d) { return codec == KVQ_CODEC_Q4_G64 ? d / 2 : d; }
 __host__ __device__ constexpr int scales_per_row(int codec, int d) { return d / group_size(codec); }
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Programmatic dependent launch: a kernel launched with launch_pdl() may start
+// while the previous kernel in the stream is finishing; pdl_wait() blocks until
+// that kernel's writes are visible and must come before the first global read
+// or write.  pdl_trigger() lets the next kernel start launching.  Both are
+// no-ops when the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // A cache plane as the kernels see it.
 struct Plane {
@@ -61,6 +88,12 @@ __host__ __device__ inline void split_range(int len, int n_splits, int split, in
 
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);
+// Tensor-core path: up to 8 query rows per kv head, head_dim 64/128/256, V in Q4_G64.
+bool decode_mma_supported(const DecodeArgs &a);
+cudaError_t launch_decode_mma(const DecodeArgs &a, int q_dtype, cudaStream_t st);
+// Tensor-core path for 9..32 query rows per kv head (MTP verify), head_dim 128/256, V in Q4_G64.
+bool decode_wide_supported(const DecodeArgs &a);
+cudaError_t launch_decode_wide(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int rows, int head_dim,
                          float *out, float *out_lse, cudaStream_t st);
 cudaError_t launch_dequant(const Plane &p, int64_t n_rows, int head_dim, float *out, cudaStream_t st);

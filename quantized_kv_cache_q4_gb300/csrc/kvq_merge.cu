@@ -5,16 +5,17 @@
 // out = sum_s w_s o_s / sum_s w_s and lse = M + ln sum_s w_s.  Parts with
 // lse = -inf (no visible key) carry no weight and their o is never read.
 //
-// One block per row.  The block first turns the n_splits lse values into
-// weights in shared memory, then each thread accumulates one float4 column
-// over a strided subset of the splits; the subsets are summed in shared
-// memory.
+// Grid (row, block of 16 float4 columns).  A block first turns the row's
+// n_splits lse values into weights in shared memory, then each thread
+// accumulates one float4 column over a strided subset of the splits (16
+// subsets); the subsets are summed in shared memory.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 16;                  // float4 columns per block
 
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_splits, int rows, int D,
@@ -26,6 +27,8 @@ merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_s
     __shared__ float s_stat[2];
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
 
     float mx = -INFINITY;
     for (int s = tid; s < n_splits; s += kMergeThreads) mx = fmaxf(mx, pl[(int64_t)s * rows + row]);
@@ -59,15 +62,17 @@ merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_s
     }
     __syncthreads();
     const float W = s_stat[1];
+    const int D4 = D / 4;
+    const int cb = blockIdx.y * kMergeCols;           // first float4 column of this block
     if (M == -INFINITY) {
-        for (int d = tid; d < D; d += kMergeThreads) out[(int64_t)row * D + d] = 0.0f;
-        if (tid == 0 && out_lse) out_lse[row] = -INFINITY;
+        for (int d = cb * 4 + tid; d < min(D, (cb + kMergeCols) * 4); d += kMergeThreads) out[(int64_t)row * D + d] = 0.0f;
+        if (tid == 0 && blockIdx.y == 0 && out_lse) out_lse[row] = -INFINITY;
         return;
     }
     const float inv = 1.0f / W;
-    const int D4 = D / 4;
-    for (int c0 = 0; c0 < D4; c0 += kMergeThreads) {
-        const int ncol = min(kMergeThreads, D4 - c0);
+    {
+        const int c0 = cb;
+        const int ncol = min(kMergeCols, D4 - c0);
         const int lanes = max(1, kMergeThreads / ncol);      // split-lanes per column
         const int col = tid % ncol, sl = tid / ncol;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -95,7 +100,7 @@ merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_s
             reinterpret_cast<float4 *>(out + (int64_t)row * D)[c0 + tid] = t;
         }
     }
-    if (tid == 0 && out_lse) out_lse[row] = M + logf(W);
+    if (tid == 0 && blockIdx.y == 0 && out_lse) out_lse[row] = M + logf(W);
 }
 
 }  // namespace
@@ -109,8 +114,9 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
         cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    merge_kernel<<<rows, kMergeThreads, smem, st>>>(po, pl, n_splits, rows, head_dim, out, out_lse);
-    return cudaGetLastError();
+    const dim3 grid((unsigned)rows, (unsigned)ceil_div(head_dim / 4, kMergeCols));
+    return launch_pdl(merge_kernel, grid, dim3(kMergeThreads), smem, st, po, pl, n_splits, rows, head_dim, out,
+                      out_lse);
 }
 
 }  // namespace kvq

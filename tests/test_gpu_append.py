@@ -33,7 +33,7 @@ def test_workload_caches_byte_exact(cfg):
 def test_wide_range_rows_byte_exact(codec, D, dtype):
     S, n_new, Hk, cap = 3, 5, 2, 64
     x = workloads.wide_range_rows(S * n_new * Hk, D, seed=D + codec, dtype=dtype).reshape(S, n_new, Hk, D)
-    pos0 = np.array([0, 17, 59], np.int32)          # the last one runs past capacity: skipped, flagged
+    pos0 = np.array([0, 17, 60], np.int32)          # 60 + 5 > 64: the last one is skipped and flagged
     c = kvq.KVCache(codec, S, Hk, D, cap)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvq.kvq_quantize_append(c, None, dev(x), None, n_new, dev(pos0), err)
