@@ -166,6 +166,31 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v,
 kvq_status kvq_merge_splits(const float *part_o, const float *part_lse, int32_t n_splits,
                             int32_t rows, int32_t head_dim, float *out, float *out_lse, void *stream);
 
+/* Decode attention that allocates nothing and takes no workspace.
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory where they decode: code enqueuing work
+ * while a CUDA graph is being captured (an allocation there is not a stream
+ * operation), engines whose memory is all owned by their own pool, and paths
+ * that cannot afford an allocation's implicit device synchronisation.
+ * Arguments, results and errors are those of kvq_decode_attention; the split
+ * scratch comes from a file-scope __device__ array of KVQ_STATIC_SCRATCH_BYTES
+ * inside libkvq.so, which every GPU that loads the library keeps until the
+ * process exits.  A call whose scratch (kvq_decode_workspace_bytes with the
+ * same arguments) exceeds that size returns KVQ_EWORKSPACE before touching the
+ * GPU.  The first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves its contents behind:
+ * nothing in it needs to start at zero, but two calls that overlap on the GPU
+ * (different streams, no ordering between them) race on it and give wrong
+ * results.  The library allocates no memory in this call. */
+#define KVQ_STATIC_SCRATCH_BYTES (8u << 20)
+size_t kvq_static_scratch_bytes(void);
+kvq_status kvq_decode_attention_static(const kvq_cache *k, const kvq_cache *v,
+                                       const void *q, int32_t q_dtype, int32_t n_q, int32_t n_heads,
+                                       float softmax_scale, const int32_t *d_kv_len, int32_t max_kv_len,
+                                       int32_t n_splits, float *out, float *out_lse, int32_t *d_err,
+                                       void *stream);
+
 /* Dequantize a whole cache to fp32 [n_seq][n_kv_heads][capacity][head_dim] on
  * the device (scale * code, exact).  For inspection and testing. */
 kvq_status kvq_dequantize(const kvq_cache *c, float *out, void *stream);

@@ -53,6 +53,8 @@ def _load():
         "kvq_decode_attention": (I32, [C, C, P, I32, I32, I32, F, P, I32, I32, P, P, P, SZ, P, P]),
         "kvq_merge_splits": (I32, [P, P, I32, I32, I32, P, P, P]),
         "kvq_dequantize": (I32, [C, P, P]),
+        "kvq_static_scratch_bytes": (SZ, []),
+        "kvq_decode_attention_static": (I32, [C, C, P, I32, I32, I32, F, P, I32, I32, P, P, P, P]),
         "kvq_status_string": (ctypes.c_char_p, [I32]),
         "kvq_last_error": (ctypes.c_char_p, []),
     }
@@ -65,7 +67,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("kvq_row_bytes", "kvq_scales_per_row", "kvq_quantize_append", "kvq_decode_default_splits",
             "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_merge_splits", "kvq_dequantize",
-            "kvq_status_string", "kvq_last_error")
+            "kvq_status_string", "kvq_last_error", "kvq_static_scratch_bytes", "kvq_decode_attention_static")
 
 
 def _check(status: int):
@@ -172,6 +174,22 @@ def kvq_decode_attention(k: KVCache, v: KVCache, q, n_q: int, n_heads: int, soft
     _check(_lib.kvq_decode_attention(k.c, v.c, _ptr(q), q_dtype, int(n_q), int(n_heads), float(softmax_scale),
                                      _ptr(d_kv_len), int(max_kv_len), int(n_splits), _ptr(out), _ptr(out_lse),
                                      _ptr(workspace), int(workspace_bytes), _ptr(d_err), _stream(stream)))
+
+
+def kvq_static_scratch_bytes() -> int:
+    return int(_lib.kvq_static_scratch_bytes())
+
+
+def kvq_decode_attention_static(k: KVCache, v: KVCache, q, n_q: int, n_heads: int, softmax_scale: float, d_kv_len,
+                                max_kv_len: int, n_splits: int, out, out_lse=None, d_err=None, stream=None,
+                                q_dtype: int | None = None):
+    """kvq_decode_attention without a workspace: the library's own static
+    device scratch is used and nothing is allocated (see include/kvq.h)."""
+    if q_dtype is None:
+        q_dtype = _dtype_code(q)
+    _check(_lib.kvq_decode_attention_static(k.c, v.c, _ptr(q), q_dtype, int(n_q), int(n_heads),
+                                            float(softmax_scale), _ptr(d_kv_len), int(max_kv_len), int(n_splits),
+                                            _ptr(out), _ptr(out_lse), _ptr(d_err), _stream(stream)))
 
 
 def kvq_merge_splits(part_o, part_lse, n_splits: int, rows: int, head_dim: int, out, out_lse=None, stream=None):

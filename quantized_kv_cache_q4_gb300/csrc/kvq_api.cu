@@ -87,6 +87,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+void kvq::set_last_error(const char *msg)
+{
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+}
+
 extern "C" {
 
 int32_t kvq_row_bytes(int32_t codec, int32_t head_dim)

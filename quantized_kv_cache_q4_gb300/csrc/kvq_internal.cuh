@@ -86,6 +86,9 @@ __host__ __device__ inline void split_range(int len, int n_splits, int split, in
     hi = (int)(h < len ? h : len);
 }
 
+// Set the message kvq_last_error() returns on the calling thread.
+void set_last_error(const char *msg);
+
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // Tensor-core path: up to 8 query rows per kv head, head_dim 64/128/256, V in Q4_G64.
