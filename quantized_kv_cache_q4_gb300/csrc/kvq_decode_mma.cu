@@ -414,6 +414,10 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
+        // two CTAs per SM need the largest shared-memory carveout
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
