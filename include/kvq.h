@@ -127,7 +127,7 @@ size_t kvq_decode_workspace_bytes(int32_t n_seq, int32_t n_kv_heads, int32_t n_h
  *   k, v          : caches with the same n_seq, n_kv_heads, head_dim, capacity.
  *                   Supported pairs: (Q4_G64, Q4_G64), (Q8_0, Q4_G64), (Q4_G64, Q8_0),
  *                   (Q8_0, Q8_0).
- *   q             : DEVICE, [n_seq][n_q][n_heads][head_dim], dtype q_dtype.
+ *   q             : DEVICE, [n_seq][n_q][n_heads][head_dim], dtype q_dtype, 16-byte aligned.
  *                   Query head h reads kv head h / (n_heads / n_kv_heads).
  *   softmax_scale : multiplies q.k (e.g. 1/sqrt(head_dim)).
  *   d_kv_len      : DEVICE int32 [n_seq], keys visible to the LAST query token

@@ -74,7 +74,11 @@ int resolve_splits(int32_t n_seq, int32_t n_kv_heads, int32_t max_kv_len, int32_
 {
     if (n_splits > 0) return n_splits;
     const int64_t units = (int64_t)n_seq * n_kv_heads;
-    const int64_t target = 2LL * sm_count();                       // two CTAs per SM
+    // one wave of CTAs (3 per SM) for a single sequence; for a batch, whose
+    // lengths may be ragged, up to four waves so that the longest sequence is
+    // cut finely enough (every sequence gets the same number of splits)
+    const int64_t waves = n_seq < 4 ? n_seq : 4;
+    const int64_t target = 3LL * sm_count() * waves;
     int64_t s = kvq::ceil_div(target, units);
     const int64_t max_useful = kvq::ceil_div(max_kv_len, 256);      // at least 256 tokens a split
     if (s > max_useful) s = max_useful;
@@ -190,6 +194,7 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const vo
         k->capacity != v->capacity)
         return fail(KVQ_EINVAL, "decode: k and v caches disagree on n_seq/n_kv_heads/head_dim/capacity");
     if (!q) return fail(KVQ_EINVAL, "decode: q is NULL");
+    if (!aligned16(q)) return fail(KVQ_EINVAL, "decode: q must be 16-byte aligned");
     if (q_dtype != KVQ_F32 && q_dtype != KVQ_F16) return fail(KVQ_EINVAL, "decode: q_dtype %d", q_dtype);
     if (n_q <= 0) return fail(KVQ_EINVAL, "decode: n_q=%d", n_q);
     if (n_heads <= 0 || n_heads % k->n_kv_heads != 0)
@@ -238,8 +243,7 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const vo
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t le;
-    if (kvq::decode_mma_supported(a)) le = kvq::launch_decode_mma(a, q_dtype, cs);
-    else if (kvq::decode_wide_supported(a)) le = kvq::launch_decode_wide(a, q_dtype, cs);
+    if (kvq::decode_tc_supported(a)) le = kvq::launch_decode_tc(a, q_dtype, cs);
     else le = kvq::launch_decode_simt(a, q_dtype, cs);
     if ((st = cuda_status(le, "decode launch")) != KVQ_OK) return st;
     if (s > 1)

@@ -1,0 +1,612 @@
+// kvq_decode_tc.cu -- split-K decode / MTP-verify attention over a packed cache
+// on the tensor cores, for 1..32 query rows per kv head (GQA group x query
+// tokens), head_dim 64/128/256, K in Q4_G64 or q8_0 and V in Q4_G64
+// (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
+// this fork is": signed INT4 + one FP16 scale per 64 values; "Results": MTP
+// n-max 2, i.e. 1 + 2 query tokens per sequence).
+//
+// Per (sequence, kv head, split) the query rows of the kv head attend to the
+// split's tokens intersected with each row's visible keys; the result is final
+// (one split) or a partial normalised over the split with its log-sum-exp.
+//
+// Work of one CTA (four warps, no dedicated producer):
+//  * Thread 0 fetches the query rows with 1D bulk copies and the first tiles of
+//    64 tokens (K and V codes by swizzled 2D TMA, their fp16 scales by bulk
+//    copies) into a 3-stage shared-memory ring.  The last warp to release a
+//    stage refills it, so no warp ever waits for a slot.
+//  * Phase A: warp w computes S^T = K Q^T for tokens [16w, 16w+16) of the tile
+//    and all n-tiles of 8 rows on mma.sync.m16n8k16.  The K codes enter as
+//    exact fp16 integers with their bias (1032 + q or 1152 + 16 q, one LOP3 per
+//    two values); each 64-value group starts its accumulator at minus the
+//    group's bias term and is scaled by the group's fp16 scale in fp32.
+//  * The per-row maximum of the tile is reduced over the CTA through shared
+//    memory, so all warps share one running maximum (online softmax in log2
+//    units); p = 2^(s - m) goes to shared memory.
+//  * Phase B: warp w owns a quarter of head_dim and accumulates O^T += V^T P'^T
+//    over the tile's 64 tokens: V^T fragments from ldmatrix.trans (it pairs two
+//    tokens at one head_dim index, the A-fragment pairing), V codes again with
+//    their fp16 bias, which a second MMA against a constant operand removes
+//    after every 16 tokens; P' = p * v_scale(token) is rounded once to fp16.
+//  * Because the warps share the maximum and each owns its own columns, the
+//    end of the CTA is a division by the row sum: no cross-warp combine.
+//
+// Every mbarrier wait is bounded: after ~1 s the kernel sets KVQ_ERR_TIMEOUT in
+// the caller's error word and finishes without further waits; nothing traps.
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+using namespace ptx;
+namespace {
+
+constexpr int kS = 3;                        // ring stages
+constexpr int kW = 4;                        // warps
+constexpr int kT = kW * 32;                  // threads
+
+__device__ __forceinline__ void warps_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kT) : "memory"); }
+
+template <int KC, int D, int NT, typename QT>
+struct TcCfg {
+    static constexpr int KRB = row_bytes(KC, D), VRB = D / 2;
+    static constexpr int KSB = 2 * scales_per_row(KC, D), VSB = 2 * (D / 64);
+    static constexpr int NGK = D / group_size(KC);
+    static constexpr int ROWS = NT * 8;                           // query rows kept (zero past R)
+    static constexpr int PS = ROWS + 4;                           // p row stride in floats (bank spread)
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = align_up(kTile * KRB, 1024);
+    static constexpr int KS_OFF = V_OFF + align_up(kTile * VRB, 1024);
+    static constexpr int VS_OFF = KS_OFF + align_up(kTile * KSB, 128);
+    static constexpr int STAGE = align_up(VS_OFF + kTile * VSB, 1024);
+    static constexpr int QP_OFF = kS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
+    static constexpr int KB_OFF = QP_OFF + ROWS * D * 2;          // fp32 [NGK][ROWS]: minus the K bias terms
+    // the query rows as given are only read before the first tile, the p tile
+    // and the reductions only after it: they share one region
+    static constexpr int U_OFF = KB_OFF + align_up(ROWS * NGK * 4, 16);
+    static constexpr int QST_OFF = U_OFF;
+    static constexpr int P_OFF = U_OFF;                                   // fp32 [64][PS]
+    static constexpr int RED_OFF = P_OFF + align_up(kTile * PS * 4, 16);  // fp32 [kW][32] x 2
+    static constexpr int QST_BYTES = ROWS * D * (int)sizeof(QT);
+    static constexpr int PR_BYTES = (RED_OFF - U_OFF) + 2 * kW * 32 * 4;
+    static constexpr int BAR_OFF = align_up(U_OFF + (QST_BYTES > PR_BYTES ? QST_BYTES : PR_BYTES), 16);
+    static constexpr int SMEM = BAR_OFF + (2 * kS + 1) * 8 + 1024;        // + alignment slack
+    static constexpr int MTW = (D / 64 * 4) / kW;                 // 16-row head_dim tiles per warp in phase B
+    // CTAs per SM the kernel is built for (shared memory allows 3 up to 16 rows)
+    static constexpr int MIN_BLOCKS = NT <= 2 ? 3 : 2;
+};
+
+// head_dim index fed by k-position kp (0..15) of k-step ks, in the order the K
+// unpack delivers values (Q4_G64: pairs (d, d + 4) of a 4-byte piece; q8_0:
+// pairs (d, d + 1)), and its inverse.
+template <int KC>
+__device__ __forceinline__ int kpos_to_d(int ks, int kp)
+{
+    const int hi = kp >> 3, t = (kp & 7) >> 1, h = kp & 1;
+    if constexpr (KC == KVQ_CODEC_Q4_G64) return 64 * (ks >> 2) + 32 * hi + 8 * t + (ks & 3) + 4 * h;
+    else return 32 * (ks >> 1) + 16 * hi + 4 * t + 2 * (ks & 1) + h;
+}
+
+template <int KC>
+__device__ __forceinline__ int d_to_kpos(int d)
+{
+    if constexpr (KC == KVQ_CODEC_Q4_G64) {
+        const int g = d >> 6, r = d & 63, hi = r >> 5, t = (r & 31) >> 3, st = r & 3, h = (r >> 2) & 1;
+        return 16 * (4 * g + st) + 8 * hi + 2 * t + h;
+    } else {
+        const int g = d >> 5, r = d & 31, hi = r >> 4, t = (r & 15) >> 2, st = (r >> 1) & 1, h = r & 1;
+        return 16 * (2 * g + st) + 8 * hi + 2 * t + h;
+    }
+}
+
+// byte offset of 16-byte chunk c of row n of the permuted query copy (D halves a row)
+template <int D>
+__device__ __forceinline__ uint32_t qp_chunk_off(int n, int c)
+{
+    return (uint32_t)(n * D * 2 + ((c ^ (n & 7)) << 4));
+}
+
+// Nibble pair e (0..3) of a code word as fp16x2 with its bias left in: pair e
+// holds nibbles e and e + 4 (the order the ldmatrix.trans fragment pairs two
+// tokens in), as 1032 + q for even e and 1152 + 16 q for odd e.
+__device__ __forceinline__ uint32_t q4_pair_biased(uint32_t w, int e)
+{
+    const uint32_t x = (e & 2) ? (w >> 8) : w;
+    return (e & 1) ? lop3_ac(x, 0x64806480u, 0x64706470u) : lop3_ac(x, 0x64086408u, 0x64076407u);
+}
+
+template <typename C, typename KG, typename VG>
+__device__ __forceinline__ void issue_tile(uint32_t base, uint32_t full, const CUtensorMap *tmk,
+                                           const CUtensorMap *tmv, const uint8_t *ksc, const uint8_t *vsc,
+                                           int64_t row0)
+{
+    mbar_expect_tx(full, (uint32_t)(KG::BYTES + VG::BYTES + kTile * (C::KSB + C::VSB)));
+    const int y = (int)row0;
+#pragma unroll
+    for (int b = 0; b < KG::NB; ++b) tma_load_2d(base + C::K_OFF + b * kTile * KG::BI, tmk, b * KG::BI, y, full);
+#pragma unroll
+    for (int b = 0; b < VG::NB; ++b) tma_load_2d(base + C::V_OFF + b * kTile * VG::BI, tmv, b * VG::BI, y, full);
+    bulk_load(base + C::KS_OFF, ksc + row0 * C::KSB, kTile * C::KSB, full);
+    bulk_load(base + C::VS_OFF, vsc + row0 * C::VSB, kTile * C::VSB, full);
+}
+
+template <int KC, int D, int NT, typename QT>
+__global__ void __launch_bounds__(kT, (TcCfg<KC, D, NT, QT>::MIN_BLOCKS))
+decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
+{
+    using C = TcCfg<KC, D, NT, QT>;
+    using KG = TileGeom<C::KRB>;
+    using VG = TileGeom<C::VRB>;
+    constexpr int NGK = C::NGK;
+    constexpr int KSTEP_PER_G = group_size(KC) / 16;
+    constexpr int MTW = C::MTW;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qp = smem + C::QP_OFF;
+    float *kb_s = reinterpret_cast<float *>(smem + C::KB_OFF);
+    float *p_s = reinterpret_cast<float *>(smem + C::P_OFF);
+    float *red_m = reinterpret_cast<float *>(smem + C::RED_OFF);      // [kW][32]
+    float *red_l = red_m + kW * 32;                                  // [kW][32]
+    const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);
+    const uint32_t bar_empty = bar_full + kS * 8;
+    const uint32_t bar_q = bar_empty + kS * 8;
+    __shared__ volatile int s_timeout;
+    __shared__ int s_issued;
+    __shared__ int s_rel[kS];
+
+    const int split = blockIdx.x, kh = blockIdx.y, s = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int R = a.n_q * G;                             // <= 8 * NT
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+        s_timeout = 0;
+        s_issued = 0;
+        for (int i = 0; i < kS; ++i) {
+            s_rel[i] = 0;
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, kW);
+        }
+        mbar_init(bar_q, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < C::ROWS * NGK; i += kT) kb_s[i] = 0.0f;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    // query rows (for each query token, the G heads of this kv head are one
+    // contiguous run) by bulk copy, in parallel with what follows
+    if (threadIdx.x == 0) {
+        const uint32_t run = (uint32_t)(G * D * sizeof(QT));
+        mbar_expect_tx(bar_q, run * (uint32_t)a.n_q);
+        const QT *q = static_cast<const QT *>(a.q);
+        for (int i = 0; i < a.n_q; ++i)
+            bulk_load(smem_u32(smem + C::QST_OFF) + i * run, q + (((int64_t)s * a.n_q + i) * a.n_heads + kh * G) * D,
+                      run, bar_q);
+    }
+
+    int len = a.kv_len[s];
+    if (len < 0 || len > a.max_kv_len) {
+        if (threadIdx.x == 0 && split == 0 && kh == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
+        len = len < 0 ? 0 : a.max_kv_len;
+    }
+    int lo, hi;
+    split_range(len, a.n_splits, split, lo, hi);
+    const int n_tiles = (int)ceil_div(hi - lo, kTile);
+    const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
+    const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
+    const uint8_t *vsc = reinterpret_cast<const uint8_t *>(a.v.sc);
+    if (threadIdx.x == 0) {
+        const int first = min(kS, n_tiles);
+        for (int j = 0; j < first; ++j)
+            issue_tile<C, KG, VG>(smem_u32(smem + j * C::STAGE), bar_full + 8 * j, &tmk, &tmv, ksc, vsc,
+                                  plane_row + lo + j * kTile);
+        s_issued = first;
+    }
+
+    // The query as fp16, head_dim permuted to the K-unpack order and swizzled for
+    // ldmatrix; with Q4_G64 K the odd head_dim indices are divided by 16 (exact
+    // for normal values) because their codes arrive as 1152 + 16 q.  Each warp
+    // step covers 32 consecutive head_dim values of one row, which lie in one
+    // K group, so the group's bias term sum_d bias(d) q(d) (bias 1032 at even,
+    // 1152 at odd d for Q4_G64; 1152 for q8_0) is a warp sum plus at most two
+    // shared-memory adds per group (commutative, hence deterministic).
+    if (!mbar_wait(bar_q, 0)) s_timeout = 1;
+    {
+        const QT *qst = reinterpret_cast<const QT *>(smem + C::QST_OFF);
+        for (int idx = threadIdx.x; idx < C::ROWS * D; idx += kT) {
+            const int n = idx / D, d = idx % D;
+            float x = 0.0f;
+            if (n < R && !s_timeout) {
+                if constexpr (sizeof(QT) == 2) x = __half2float(qst[idx]);
+                else x = __half2float(__float2half_rn(qst[idx]));
+            }
+            if constexpr (KC == KVQ_CODEC_Q4_G64)
+                if (d & 1) x *= 0.0625f;
+            const __half h = __float2half_rn(x);
+            const int kg = d_to_kpos<KC>(d);
+            *reinterpret_cast<__half *>(qp + qp_chunk_off<D>(n, kg >> 3) + (kg & 7) * 2) = h;
+            float b = __half2float(h) * ((KC == KVQ_CODEC_Q4_G64 && (d & 1) == 0) ? 1032.0f : 1152.0f);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
+            if (lane == 0) atomicAdd(&kb_s[(d / group_size(KC)) * C::ROWS + n], -b);
+        }
+    }
+    __syncthreads();
+
+    int nv[NT][2];
+    int nv_min = 0x7FFFFFFF;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int r = nt * 8 + 2 * tig + c;
+            nv[nt][c] = r < R ? len - a.n_q + r / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
+            nv_min = min(nv_min, nv[nt][c]);
+        }
+    const float sl2 = a.scale_log2;
+    const int tl = warp * 16;                                           // phase A tokens
+    // phase B head_dim slice: group g_w, nibble pairs e0 .. e0 + MTW - 1 of each code word
+    const int g_w = (warp * MTW) / 4, e0 = (MTW == 4) ? 0 : (warp * MTW) % 4;
+    uint32_t koff[NGK];
+    {
+        const int ktok = tl + (lane & 7) + 8 * ((lane >> 3) & 1), kch = lane >> 4;
+#pragma unroll
+        for (int g = 0; g < NGK; ++g) koff[g] = KG::chunk_addr(C::K_OFF, ktok, 2 * g + kch);
+    }
+    const uint32_t voff0 = VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), 2 * g_w + ((lane >> 3) & 1));
+    const uint32_t qp_base = smem_u32(qp);
+
+    float o[MTW][NT][4];
+#pragma unroll
+    for (int t = 0; t < MTW; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[t][nt][c] = 0.0f;
+    float m[NT][2], l[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.0f;
+
+    for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kS;
+        if (!s_timeout && !mbar_wait(bar_full + 8 * st, (j / kS) & 1)) s_timeout = 1;
+        // the barriers below need all four warps every tile: after a timeout the
+        // warps keep stepping with masked data instead of leaving
+        const bool dead = s_timeout != 0;
+        const int t_tile = lo + j * kTile;
+        const int tb = t_tile + tl;
+        const uint32_t base = smem_u32(smem + st * C::STAGE);
+        const uint8_t *ksp = smem + st * C::STAGE + C::KS_OFF;
+        const uint8_t *vsp = smem + st * C::STAGE + C::VS_OFF;
+
+        // ---- phase A: S^T for this warp's 16 tokens ----
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[nt][c] = 0.0f;
+        if (tb < hi && !dead) {
+            float sk0[NGK], sk1[NGK];
+            load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
+            load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
+#pragma unroll
+            for (int g = 0; g < NGK; ++g) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(base + koff[g], r0, r1, r2, r3);
+                uint32_t h0[4], h1[4], h2[4], h3[4];
+                if constexpr (KC == KVQ_CODEC_Q4_G64) {
+                    unpack_q4_biased(r0, h0);
+                    unpack_q4_biased(r1, h1);
+                    unpack_q4_biased(r2, h2);
+                    unpack_q4_biased(r3, h3);
+                } else {
+                    uint32_t t2[2];
+                    unpack_q8_biased(r0, t2); h0[0] = t2[0]; h0[1] = t2[1];
+                    unpack_q8_biased(r1, t2); h1[0] = t2[0]; h1[1] = t2[1];
+                    unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
+                    unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
+                }
+                // each group's accumulator starts at minus its bias term
+                float cg[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float2 nb2 = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
+                    cg[nt][0] = nb2.x;
+                    cg[nt][1] = nb2.y;
+                    cg[nt][2] = nb2.x;
+                    cg[nt][3] = nb2.y;
+                }
+#pragma unroll
+                for (int k = 0; k < KSTEP_PER_G; ++k) {
+                    const int ks = g * KSTEP_PER_G + k;
+#pragma unroll
+                    for (int np = 0; np < (NT + 1) / 2; ++np) {
+                        // B fragments of n-tiles 2np and 2np+1 (the second exists only
+                        // when 2np + 1 < NT)
+                        uint32_t b00, b01, b10, b11;
+                        if (2 * np + 1 < NT) {
+                            const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
+                            ldsm_x4(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
+                        } else {
+                            const int qrow = 2 * np * 8 + (lane & 7);
+                            ldsm_x2(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
+                            b10 = b11 = 0u;
+                        }
+                        mma16816(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01);
+                        if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    sc[nt][0] = fmaf(cg[nt][0], sk0[g], sc[nt][0]);
+                    sc[nt][1] = fmaf(cg[nt][1], sk0[g], sc[nt][1]);
+                    sc[nt][2] = fmaf(cg[nt][2], sk1[g], sc[nt][2]);
+                    sc[nt][3] = fmaf(cg[nt][3], sk1[g], sc[nt][3]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[nt][c] *= sl2;
+        }
+        {
+            const int ta = tb + gid, tc = ta + 8;
+            if (dead || tb + 16 > hi || tb + 16 > nv_min) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (dead || !(ta < hi && ta < nv[nt][0])) sc[nt][0] = -INFINITY;
+                    if (dead || !(ta < hi && ta < nv[nt][1])) sc[nt][1] = -INFINITY;
+                    if (dead || !(tc < hi && tc < nv[nt][0])) sc[nt][2] = -INFINITY;
+                    if (dead || !(tc < hi && tc < nv[nt][1])) sc[nt][3] = -INFINITY;
+                }
+            }
+        }
+        // ---- the tile's maximum per row over the CTA ----
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float mx0 = fmaxf(sc[nt][0], sc[nt][2]), mx1 = fmaxf(sc[nt][1], sc[nt][3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            if (gid == 0) {
+                red_m[warp * 32 + nt * 8 + 2 * tig] = mx0;
+                red_m[warp * 32 + nt * 8 + 2 * tig + 1] = mx1;
+            }
+        }
+        warps_sync();
+        float corr[NT][2];
+        bool grow = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int col = nt * 8 + 2 * tig + c;
+                float tmax = red_m[col];
+#pragma unroll
+                for (int w = 1; w < kW; ++w) tmax = fmaxf(tmax, red_m[w * 32 + col]);
+                const float mn = fmaxf(m[nt][c], tmax);
+                corr[nt][c] = (mn == -INFINITY) ? 1.0f : ex2(m[nt][c] - mn);
+                grow |= mn > m[nt][c];
+                m[nt][c] = mn;
+            }
+        // p of this warp's tokens for phase B (0 for masked tokens)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float ms0 = (m[nt][0] == -INFINITY) ? 0.0f : m[nt][0];
+            const float ms1 = (m[nt][1] == -INFINITY) ? 0.0f : m[nt][1];
+            const float p0 = ex2(sc[nt][0] - ms0), p1 = ex2(sc[nt][1] - ms1);
+            const float p2 = ex2(sc[nt][2] - ms0), p3 = ex2(sc[nt][3] - ms1);
+            l[nt][0] = l[nt][0] * corr[nt][0] + p0 + p2;
+            l[nt][1] = l[nt][1] * corr[nt][1] + p1 + p3;
+            *reinterpret_cast<float2 *>(p_s + (tl + gid) * C::PS + nt * 8 + 2 * tig) = make_float2(p0, p1);
+            *reinterpret_cast<float2 *>(p_s + (tl + gid + 8) * C::PS + nt * 8 + 2 * tig) = make_float2(p2, p3);
+        }
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+            for (int t = 0; t < MTW; ++t)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    o[t][nt][0] *= corr[nt][0];
+                    o[t][nt][1] *= corr[nt][1];
+                    o[t][nt][2] *= corr[nt][0];
+                    o[t][nt][3] *= corr[nt][1];
+                }
+        }
+        warps_sync();
+
+        // ---- phase B: O^T += V^T P'^T over the tile, this warp's head_dim slice ----
+        if (!dead) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                if (t_tile + 16 * kk >= hi) break;
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
+                // V scales of the four tokens of this lane's B fragment (0 past the split end)
+                float sv[4];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int tk = 16 * kk + 2 * tig + (qq & 1) + 8 * (qq >> 1);
+                    sv[qq] = (t_tile + tk < hi) ? __half2float(reinterpret_cast<const __half *>(vsp + tk * C::VSB)[g_w])
+                                                : 0.0f;
+                }
+                uint32_t b0[NT], b1[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float *pr = p_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
+                    b0[nt] = pack_f16x2(pr[0] * sv[0], pr[C::PS] * sv[1]);
+                    b1[nt] = pack_f16x2(pr[8 * C::PS] * sv[2], pr[9 * C::PS] * sv[3]);
+                }
+#pragma unroll
+                for (int t = 0; t < MTW; ++t) {
+                    const int e = e0 + t;
+                    const uint32_t a0 = q4_pair_biased(r0, e), a1 = q4_pair_biased(r1, e);
+                    const uint32_t a2 = q4_pair_biased(r2, e), a3 = q4_pair_biased(r3, e);
+                    const uint32_t nb = (e & 1) ? 0xE480E480u : 0xE408E408u;   // fp16x2 -1152 / -1032
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma16816(o[t][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+                        mma16816(o[t][nt], nb, nb, nb, nb, b0[nt], b1[nt]);
+                    }
+                }
+            }
+        }
+        // release the stage; the last warp to release it refills it with tile j + kS
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(bar_empty + 8 * st);
+            if (atomicAdd(&s_rel[st], 1) == kW - 1) {
+                s_rel[st] = 0;
+                const int jn = j + kS;
+                if (jn < n_tiles && !s_timeout) {
+                    // completes at once (this was the stage's last release) and orders
+                    // the other warps' reads of the stage before the refill
+                    if (mbar_wait(bar_empty + 8 * st, (j / kS) & 1)) {
+                        issue_tile<C, KG, VG>(base, bar_full + 8 * st, &tmk, &tmv, ksc, vsc,
+                                              plane_row + lo + jn * kTile);
+                        atomicMax(&s_issued, jn + 1);
+                    } else {
+                        s_timeout = 1;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- row sums over the CTA, then each warp writes its head_dim slice ----
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+        }
+    if (gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            red_l[warp * 32 + nt * 8 + 2 * tig] = l[nt][0];
+            red_l[warp * 32 + nt * 8 + 2 * tig + 1] = l[nt][1];
+        }
+    }
+    __syncthreads();
+    // never leave while a copy into this CTA's shared memory could be in flight
+    // (only possible after a timeout; otherwise every issued copy was waited on)
+    if (threadIdx.x == 0 && s_timeout) {
+        const int issued = s_issued;
+        for (int j = issued - 1; j >= 0 && j >= issued - kS; --j) mbar_wait(bar_full + 8 * (j % kS), (j / kS) & 1);
+        mbar_wait(bar_q, 0);
+    }
+    const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int n = nt * 8 + 2 * tig + (c & 1);
+            if (n >= R) continue;
+            float L = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kW; ++w) L += red_l[w * 32 + n];
+            const float M = m[nt][c & 1];
+            const bool empty = (M == -INFINITY || L <= 0.0f);
+            const float inv = empty ? 0.0f : 1.0f / L;
+            const int i = n / G, jj = n % G;
+            const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
+            float *dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
+            const int d = 64 * g_w + 32 * (c >> 1) + 4 * gid + e0;
+            float v[MTW];
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+                // rows of odd head_dim index were accumulated 16x (their codes' 1152 + 16 q form)
+                const int e = e0 + t;
+                v[t] = o[t][nt][c] * inv * ((e & 1) ? 0.0625f : 1.0f);
+            }
+            if constexpr (MTW == 4) *reinterpret_cast<float4 *>(dst + d) = make_float4(v[0], v[1], v[2], v[3]);
+            else if constexpr (MTW == 2) *reinterpret_cast<float2 *>(dst + d) = make_float2(v[0], v[1]);
+            else dst[d] = v[0];
+            if (warp == 0 && gid == 0 && (c >> 1) == 0) {
+                const float lse = empty ? -INFINITY : (M + log2f(L)) * kLn2;
+                if (a.n_splits == 1) {
+                    if (a.out_lse) a.out_lse[orow] = lse;
+                } else {
+                    a.part_lse[(int64_t)split * rows_total + orow] = lse;
+                }
+            }
+        }
+    if (threadIdx.x == 0 && s_timeout && a.err) atomicOr(a.err, KVQ_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int KC, int D, int NT, typename QT>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
+{
+    using C = TcCfg<KC, D, NT, QT>;
+    static_assert(C::SMEM <= 227 * 1024, "shared memory of one CTA");
+    const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
+    CUtensorMap tk, tv;
+    if (!make_codes_map(&tk, a.k.qs, C::KRB, rows) || !make_codes_map(&tv, a.v.qs, C::VRB, rows))
+        return cudaErrorInvalidValue;
+    auto kern = decode_tc_kernel<KC, D, NT, QT>;
+    static bool attr_set[64] = {};           // the attributes are per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
+    return launch_pdl(kern, grid, dim3(kT), C::SMEM, st, a, tk, tv);
+}
+
+template <int KC, int D, typename QT>
+cudaError_t launch_nt(const DecodeArgs &a, cudaStream_t st)
+{
+    const int R = a.n_q * (a.n_heads / a.n_kv_heads);
+    switch ((R + 7) / 8) {
+    case 1: return launch_t<KC, D, 1, QT>(a, st);
+    case 2: return launch_t<KC, D, 2, QT>(a, st);
+    case 3: return launch_t<KC, D, 3, QT>(a, st);
+    case 4: return launch_t<KC, D, 4, QT>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int KC, typename QT>
+cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st)
+{
+    switch (a.head_dim) {
+    case 64: return launch_nt<KC, 64, QT>(a, st);
+    case 128: return launch_nt<KC, 128, QT>(a, st);
+    case 256: return launch_nt<KC, 256, QT>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool decode_tc_supported(const DecodeArgs &a)
+{
+    const int R = a.n_q * (a.n_heads / a.n_kv_heads);
+    const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
+    return R >= 1 && R <= 32 && a.v.codec == KVQ_CODEC_Q4_G64 &&
+           (a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256) && rows < (1LL << 31) &&
+           tensor_maps_available();
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st)
+{
+    const bool k4 = a.k.codec == KVQ_CODEC_Q4_G64;
+    if (q_dtype == KVQ_F16)
+        return k4 ? launch_d<KVQ_CODEC_Q4_G64, __half>(a, st) : launch_d<KVQ_CODEC_Q8_0, __half>(a, st);
+    return k4 ? launch_d<KVQ_CODEC_Q4_G64, float>(a, st) : launch_d<KVQ_CODEC_Q8_0, float>(a, st);
+}
+
+}  // namespace kvq

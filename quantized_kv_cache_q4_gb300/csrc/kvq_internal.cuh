@@ -91,12 +91,9 @@ void set_last_error(const char *msg);
 
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);
-// Tensor-core path: up to 8 query rows per kv head, head_dim 64/128/256, V in Q4_G64.
-bool decode_mma_supported(const DecodeArgs &a);
-cudaError_t launch_decode_mma(const DecodeArgs &a, int q_dtype, cudaStream_t st);
-// Tensor-core path for 9..32 query rows per kv head (MTP verify), head_dim 128/256, V in Q4_G64.
-bool decode_wide_supported(const DecodeArgs &a);
-cudaError_t launch_decode_wide(const DecodeArgs &a, int q_dtype, cudaStream_t st);
+// Tensor-core path: 1..32 query rows per kv head, head_dim 64/128/256, V in Q4_G64.
+bool decode_tc_supported(const DecodeArgs &a);
+cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int rows, int head_dim,
                          float *out, float *out_lse, cudaStream_t st);
 cudaError_t launch_dequant(const Plane &p, int64_t n_rows, int head_dim, float *out, cudaStream_t st);

@@ -12,9 +12,6 @@ namespace kvq {
 namespace ptx {
 
 constexpr int kTile = 64;          // tokens per pipeline stage
-constexpr int kStages = 4;
-constexpr int kConsumerWarps = 4;  // 16 tokens of a tile each
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr long long kWaitCycles = 1LL << 31;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -80,6 +77,11 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
@@ -153,6 +155,54 @@ __device__ __forceinline__ void unpack_q8(uint32_t w, uint32_t (&h)[2])
     asm("prmt.b32 %0, %1, %2, 0x7342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
     h[0] = h2_as_u32(__hsub2(u32_as_h2(a), k1152));
     h[1] = h2_as_u32(__hsub2(u32_as_h2(b), k1152));
+}
+
+// The same codes with their fp16 bias left in, for operands whose bias is
+// removed after the MMA: h[0], h[2] = 1032 + q (nibble positions 0,4 and 2,6,
+// the even head_dim indices), h[1], h[3] = 1152 + 16 q (the odd indices).
+// One LOP3 per two values.
+__device__ __forceinline__ void unpack_q4_biased(uint32_t w, uint32_t (&h)[4])
+{
+    const uint32_t w8 = w >> 8;
+    h[0] = lop3_ac(w, 0x64086408u, 0x64076407u);
+    h[1] = lop3_ac(w, 0x64806480u, 0x64706470u);
+    h[2] = lop3_ac(w8, 0x64086408u, 0x64076407u);
+    h[3] = lop3_ac(w8, 0x64806480u, 0x64706470u);
+}
+
+// int8 codes as 1152 + q (byte b becomes 0x64 : (b ^ 0x80)), pairs (b0, b1), (b2, b3).
+__device__ __forceinline__ void unpack_q8_biased(uint32_t w, uint32_t (&h)[2])
+{
+    const uint32_t x = w ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(h[0]) : "r"(x), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x7342;" : "=r"(h[1]) : "r"(x), "r"(0x64646464u));
+}
+
+// NG consecutive fp16 scales at p (2*NG bytes, naturally aligned) as floats, with
+// the widest shared-memory load that fits.
+template <int NG>
+__device__ __forceinline__ void load_scales(const uint8_t *p, float (&out)[NG])
+{
+    if constexpr (NG == 1) {
+        out[0] = __half2float(*reinterpret_cast<const __half *>(p));
+    } else if constexpr (NG == 2) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(p));
+        out[0] = f.x; out[1] = f.y;
+    } else if constexpr (NG == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const float2 a = __half22float2(u32_as_h2(u.x)), b = __half22float2(u32_as_h2(u.y));
+        out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+    } else {
+        static_assert(NG % 8 == 0, "");
+#pragma unroll
+        for (int k = 0; k < NG; k += 8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(p + 2 * k);
+            const float2 a = __half22float2(u32_as_h2(u.x)), b = __half22float2(u32_as_h2(u.y));
+            const float2 c = __half22float2(u32_as_h2(u.z)), d = __half22float2(u32_as_h2(u.w));
+            out[k] = a.x; out[k + 1] = a.y; out[k + 2] = b.x; out[k + 3] = b.y;
+            out[k + 4] = c.x; out[k + 5] = c.y; out[k + 6] = d.x; out[k + 7] = d.y;
+        }
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
