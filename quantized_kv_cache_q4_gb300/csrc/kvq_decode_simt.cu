@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.n_heads / a.n_kv_heads;
     const int R = a.n_q * G;
+    // no early trigger: a dependent merge launch starts once this grid ends
     pdl_wait();
-    pdl_trigger();
 
     int len = a.kv_len[s];
     if (len < 0 || len > a.max_kv_len) {

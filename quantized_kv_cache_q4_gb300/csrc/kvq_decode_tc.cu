@@ -9,24 +9,26 @@
 // split's tokens intersected with each row's visible keys; the result is final
 // (one split) or a partial normalised over the split with its log-sum-exp.
 //
-// Work of one CTA (four warps, no dedicated producer):
+// Work of one CTA (four warps, no dedicated producer), one CTA barrier per tile:
 //  * Thread 0 fetches the query rows with 1D bulk copies and the first tiles of
 //    64 tokens (K and V codes by swizzled 2D TMA, their fp16 scales by bulk
-//    copies) into a 3-stage shared-memory ring.  The last warp to release a
-//    stage refills it, so no warp ever waits for a slot.
+//    copies) into a 3-stage shared-memory ring.  After the barrier of tile j it
+//    refills the stage of tile j - 1, which every warp has finished with.
 //  * Phase A: warp w computes S^T = K Q^T for tokens [16w, 16w+16) of the tile
 //    and all n-tiles of 8 rows on mma.sync.m16n8k16.  The K codes enter as
 //    exact fp16 integers with their bias (1032 + q or 1152 + 16 q, one LOP3 per
 //    two values); each 64-value group starts its accumulator at minus the
-//    group's bias term and is scaled by the group's fp16 scale in fp32.
-//  * The per-row maximum of the tile is reduced over the CTA through shared
-//    memory, so all warps share one running maximum (online softmax in log2
-//    units); p = 2^(s - m) goes to shared memory.
-//  * Phase B: warp w owns a quarter of head_dim and accumulates O^T += V^T P'^T
-//    over the tile's 64 tokens: V^T fragments from ldmatrix.trans (it pairs two
-//    tokens at one head_dim index, the A-fragment pairing), V codes again with
-//    their fp16 bias, which a second MMA against a constant operand removes
-//    after every 16 tokens; P' = p * v_scale(token) is rounded once to fp16.
+//    group's bias term and is scaled by the group's fp16 scale in fp32.  The
+//    scores (log2 units) and the warp's per-row maximum go to shared memory
+//    (double-buffered by tile parity, so one barrier per tile suffices).
+//  * Phase B: every warp forms the same new running maximum from the four
+//    warps' maxima, turns the scores of its operand fragments into
+//    p = 2^(s - m) (keeping the row sums itself) and accumulates
+//    O^T += V^T P'^T for its quarter of head_dim over the tile's 64 tokens:
+//    V^T fragments from ldmatrix.trans (it pairs two tokens at one head_dim
+//    index, the A-fragment pairing), V codes again with their fp16 bias, which
+//    a second MMA against a constant operand removes after every 16 tokens;
+//    P' = p * v_scale(token) is rounded once to fp16.
 //  * Because the warps share the maximum and each owns its own columns, the
 //    end of the CTA is a division by the row sum: no cross-warp combine.
 //
@@ -50,7 +52,7 @@ struct TcCfg {
     static constexpr int KSB = 2 * scales_per_row(KC, D), VSB = 2 * (D / 64);
     static constexpr int NGK = D / group_size(KC);
     static constexpr int ROWS = NT * 8;                           // query rows kept (zero past R)
-    static constexpr int PS = ROWS + 4;                           // p row stride in floats (bank spread)
+    static constexpr int PS = ROWS + 4;                           // score row stride in floats (bank spread)
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = align_up(kTile * KRB, 1024);
     static constexpr int KS_OFF = V_OFF + align_up(kTile * VRB, 1024);
@@ -58,16 +60,16 @@ struct TcCfg {
     static constexpr int STAGE = align_up(VS_OFF + kTile * VSB, 1024);
     static constexpr int QP_OFF = kS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
     static constexpr int KB_OFF = QP_OFF + ROWS * D * 2;          // fp32 [NGK][ROWS]: minus the K bias terms
-    // the query rows as given are only read before the first tile, the p tile
-    // and the reductions only after it: they share one region
+    // the query rows as given are only read before the first tile, the score
+    // tiles and the maxima only after it: they share one region
     static constexpr int U_OFF = KB_OFF + align_up(ROWS * NGK * 4, 16);
     static constexpr int QST_OFF = U_OFF;
-    static constexpr int P_OFF = U_OFF;                                   // fp32 [64][PS]
-    static constexpr int RED_OFF = P_OFF + align_up(kTile * PS * 4, 16);  // fp32 [kW][32] x 2
+    static constexpr int S_OFF = U_OFF;                                   // fp32 [2][64][PS] scores
+    static constexpr int RED_OFF = S_OFF + align_up(2 * kTile * PS * 4, 16);  // fp32 [2][kW][32] maxima
     static constexpr int QST_BYTES = ROWS * D * (int)sizeof(QT);
     static constexpr int PR_BYTES = (RED_OFF - U_OFF) + 2 * kW * 32 * 4;
     static constexpr int BAR_OFF = align_up(U_OFF + (QST_BYTES > PR_BYTES ? QST_BYTES : PR_BYTES), 16);
-    static constexpr int SMEM = BAR_OFF + (2 * kS + 1) * 8 + 1024;        // + alignment slack
+    static constexpr int SMEM = BAR_OFF + (kS + 1) * 8 + 1024;            // + alignment slack
     static constexpr int MTW = (D / 64 * 4) / kW;                 // 16-row head_dim tiles per warp in phase B
     // CTAs per SM the kernel is built for (shared memory allows 3 up to 16 rows)
     static constexpr int MIN_BLOCKS = NT <= 2 ? 3 : 2;
@@ -142,15 +144,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *qp = smem + C::QP_OFF;
     float *kb_s = reinterpret_cast<float *>(smem + C::KB_OFF);
-    float *p_s = reinterpret_cast<float *>(smem + C::P_OFF);
-    float *red_m = reinterpret_cast<float *>(smem + C::RED_OFF);      // [kW][32]
-    float *red_l = red_m + kW * 32;                                  // [kW][32]
+    float *s_s0 = reinterpret_cast<float *>(smem + C::S_OFF);        // [2][64][PS]
+    float *red_m0 = reinterpret_cast<float *>(smem + C::RED_OFF);    // [2][kW][32]
     const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);
-    const uint32_t bar_empty = bar_full + kS * 8;
-    const uint32_t bar_q = bar_empty + kS * 8;
+    const uint32_t bar_q = bar_full + kS * 8;
     __shared__ volatile int s_timeout;
     __shared__ int s_issued;
-    __shared__ int s_rel[kS];
 
     const int split = blockIdx.x, kh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,18 +161,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
         s_timeout = 0;
         s_issued = 0;
-        for (int i = 0; i < kS; ++i) {
-            s_rel[i] = 0;
-            mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, kW);
-        }
+        for (int i = 0; i < kS; ++i) mbar_init(bar_full + 8 * i, 1);
         mbar_init(bar_q, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = threadIdx.x; i < C::ROWS * NGK; i += kT) kb_s[i] = 0.0f;
     __syncthreads();
     pdl_wait();
-    pdl_trigger();
     // query rows (for each query token, the G heads of this kv head are one
     // contiguous run) by bulk copy, in parallel with what follows
     if (threadIdx.x == 0) {
@@ -206,30 +199,47 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 
     // The query as fp16, head_dim permuted to the K-unpack order and swizzled for
     // ldmatrix; with Q4_G64 K the odd head_dim indices are divided by 16 (exact
-    // for normal values) because their codes arrive as 1152 + 16 q.  Each warp
-    // step covers 32 consecutive head_dim values of one row, which lie in one
-    // K group, so the group's bias term sum_d bias(d) q(d) (bias 1032 at even,
-    // 1152 at odd d for Q4_G64; 1152 for q8_0) is a warp sum plus at most two
-    // shared-memory adds per group (commutative, hence deterministic).
+    // for normal values) because their codes arrive as 1152 + 16 q.  Each thread
+    // builds whole 16-byte chunks (8 k-positions of one k-step, so of one K
+    // group); the CPG chunks of a group sit in consecutive lanes, whose shuffle
+    // sum gives the group's bias term sum_d bias(d) q(d) (bias 1032 at even,
+    // 1152 at odd d for Q4_G64; 1152 for q8_0).
     if (!mbar_wait(bar_q, 0)) s_timeout = 1;
     {
+        constexpr int CPR = D / 8;                     // chunks per row
+        constexpr int CPG = group_size(KC) / 8;        // chunks per K group
         const QT *qst = reinterpret_cast<const QT *>(smem + C::QST_OFF);
-        for (int idx = threadIdx.x; idx < C::ROWS * D; idx += kT) {
-            const int n = idx / D, d = idx % D;
-            float x = 0.0f;
-            if (n < R && !s_timeout) {
-                if constexpr (sizeof(QT) == 2) x = __half2float(qst[idx]);
-                else x = __half2float(__float2half_rn(qst[idx]));
-            }
-            if constexpr (KC == KVQ_CODEC_Q4_G64)
-                if (d & 1) x *= 0.0625f;
-            const __half h = __float2half_rn(x);
-            const int kg = d_to_kpos<KC>(d);
-            *reinterpret_cast<__half *>(qp + qp_chunk_off<D>(n, kg >> 3) + (kg & 7) * 2) = h;
-            float b = __half2float(h) * ((KC == KVQ_CODEC_Q4_G64 && (d & 1) == 0) ? 1032.0f : 1152.0f);
+        const bool ok = !s_timeout;
+        for (int ci = threadIdx.x; ci < C::ROWS * CPR; ci += kT) {    // whole warps per step
+            const int n = ci / CPR, c = ci % CPR;
+            float x[8];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
-            if (lane == 0) atomicAdd(&kb_s[(d / group_size(KC)) * C::ROWS + n], -b);
+            for (int j = 0; j < 8; ++j) {
+                const int kg = 8 * c + j;
+                const int d = kpos_to_d<KC>(kg >> 4, kg & 15);
+                x[j] = 0.0f;
+                if (n < R && ok) {
+                    if constexpr (sizeof(QT) == 2) x[j] = __half2float(qst[n * D + d]);
+                    else x[j] = __half2float(__float2half_rn(qst[n * D + d]));
+                }
+                if constexpr (KC == KVQ_CODEC_Q4_G64)
+                    if (d & 1) x[j] *= 0.0625f;
+            }
+            uint32_t hw[4];
+            float b = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                hw[j] = pack_f16x2(x[2 * j], x[2 * j + 1]);
+                const float2 hf = __half22float2(u32_as_h2(hw[j]));
+                // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
+                const int kg = 8 * c + 2 * j;
+                const bool even = (KC == KVQ_CODEC_Q4_G64) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
+                b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
+            }
+            *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+#pragma unroll
+            for (int off = 1; off < CPG; off <<= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
+            if (c % CPG == 0) kb_s[(c / CPG) * C::ROWS + n] = -b;
         }
     }
     __syncthreads();
@@ -264,21 +274,25 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) o[t][nt][c] = 0.0f;
-    float m[NT][2], l[NT][2];
+    // running maximum and (partial) sum of row nt * 8 + gid, the row this lane's
+    // phase-B operand fragments belong to; every warp holds the same maxima
+    float mg[NT], lg[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.0f;
+    for (int nt = 0; nt < NT; ++nt) mg[nt] = -INFINITY, lg[nt] = 0.0f;
 
     for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kS;
         if (!s_timeout && !mbar_wait(bar_full + 8 * st, (j / kS) & 1)) s_timeout = 1;
-        // the barriers below need all four warps every tile: after a timeout the
+        // the barrier below needs all four warps every tile: after a timeout the
         // warps keep stepping with masked data instead of leaving
-        const bool dead = s_timeout != 0;
+        const bool dead = __any_sync(0xffffffffu, s_timeout != 0);
         const int t_tile = lo + j * kTile;
         const int tb = t_tile + tl;
         const uint32_t base = smem_u32(smem + st * C::STAGE);
         const uint8_t *ksp = smem + st * C::STAGE + C::KS_OFF;
         const uint8_t *vsp = smem + st * C::STAGE + C::VS_OFF;
+        float *s_s = s_s0 + (j & 1) * (kTile * C::PS);
+        float *red_m = red_m0 + (j & 1) * (kW * 32);
 
         // ---- phase A: S^T for this warp's 16 tokens ----
         float sc[NT][4];
@@ -362,69 +376,73 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 }
             }
         }
-        // ---- the tile's maximum per row over the CTA ----
+        // scores and this warp's per-row maximum of the tile, for phase B
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            *reinterpret_cast<float2 *>(s_s + (tl + gid) * C::PS + nt * 8 + 2 * tig) = make_float2(sc[nt][0], sc[nt][1]);
+            *reinterpret_cast<float2 *>(s_s + (tl + gid + 8) * C::PS + nt * 8 + 2 * tig) =
+                make_float2(sc[nt][2], sc[nt][3]);
             float mx0 = fmaxf(sc[nt][0], sc[nt][2]), mx1 = fmaxf(sc[nt][1], sc[nt][3]);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             }
-            if (gid == 0) {
-                red_m[warp * 32 + nt * 8 + 2 * tig] = mx0;
-                red_m[warp * 32 + nt * 8 + 2 * tig + 1] = mx1;
+            if (gid == 0) *reinterpret_cast<float2 *>(red_m + warp * 32 + nt * 8 + 2 * tig) = make_float2(mx0, mx1);
+        }
+        // The one barrier of the tile.  It also orders every warp's reads of
+        // tile j - 1 (previous phase B) before the refill of that tile's stage.
+        warps_sync();
+        if (threadIdx.x == 0 && j >= 1 && !s_timeout) {
+            const int jn = j - 1 + kS;
+            if (jn < n_tiles) {
+                issue_tile<C, KG, VG>(smem_u32(smem + ((j - 1) % kS) * C::STAGE), bar_full + 8 * ((j - 1) % kS), &tmk,
+                                      &tmv, ksc, vsc, plane_row + lo + jn * kTile);
+                s_issued = jn + 1;
             }
         }
-        warps_sync();
-        float corr[NT][2];
+
+        // ---- phase B: softmax of the tile and O^T += V^T P'^T for this warp's head_dim slice ----
+        // new running maximum of row nt * 8 + gid (the same in every warp)
+        float cf[NT];
         bool grow = false;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int col = nt * 8 + 2 * tig + c;
-                float tmax = red_m[col];
-#pragma unroll
-                for (int w = 1; w < kW; ++w) tmax = fmaxf(tmax, red_m[w * 32 + col]);
-                const float mn = fmaxf(m[nt][c], tmax);
-                corr[nt][c] = (mn == -INFINITY) ? 1.0f : ex2(m[nt][c] - mn);
-                grow |= mn > m[nt][c];
-                m[nt][c] = mn;
-            }
-        // p of this warp's tokens for phase B (0 for masked tokens)
-#pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float ms0 = (m[nt][0] == -INFINITY) ? 0.0f : m[nt][0];
-            const float ms1 = (m[nt][1] == -INFINITY) ? 0.0f : m[nt][1];
-            const float p0 = ex2(sc[nt][0] - ms0), p1 = ex2(sc[nt][1] - ms1);
-            const float p2 = ex2(sc[nt][2] - ms0), p3 = ex2(sc[nt][3] - ms1);
-            l[nt][0] = l[nt][0] * corr[nt][0] + p0 + p2;
-            l[nt][1] = l[nt][1] * corr[nt][1] + p1 + p3;
-            *reinterpret_cast<float2 *>(p_s + (tl + gid) * C::PS + nt * 8 + 2 * tig) = make_float2(p0, p1);
-            *reinterpret_cast<float2 *>(p_s + (tl + gid + 8) * C::PS + nt * 8 + 2 * tig) = make_float2(p2, p3);
+            const int r = nt * 8 + gid;
+            float tmax = red_m[r];
+#pragma unroll
+            for (int w = 1; w < kW; ++w) tmax = fmaxf(tmax, red_m[w * 32 + r]);
+            const float mn = fmaxf(mg[nt], tmax);
+            cf[nt] = (mn == -INFINITY) ? 1.0f : ex2(mg[nt] - mn);
+            grow |= mn > mg[nt];
+            mg[nt] = mn;
+            lg[nt] *= cf[nt];
         }
         if (__any_sync(0xffffffffu, grow)) {
+            // accumulator columns are rows 2 tig and 2 tig + 1: their factors come from
+            // the lanes whose fragment row they are
 #pragma unroll
-            for (int t = 0; t < MTW; ++t)
+            for (int nt = 0; nt < NT; ++nt) {
+                const float c0 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig);
+                const float c1 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig + 4);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    o[t][nt][0] *= corr[nt][0];
-                    o[t][nt][1] *= corr[nt][1];
-                    o[t][nt][2] *= corr[nt][0];
-                    o[t][nt][3] *= corr[nt][1];
+                for (int t = 0; t < MTW; ++t) {
+                    o[t][nt][0] *= c0;
+                    o[t][nt][1] *= c1;
+                    o[t][nt][2] *= c0;
+                    o[t][nt][3] *= c1;
                 }
+            }
         }
-        warps_sync();
-
-        // ---- phase B: O^T += V^T P'^T over the tile, this warp's head_dim slice ----
         if (!dead) {
+            float msub[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
-                if (t_tile + 16 * kk >= hi) break;
+                // tokens past the split end have score -inf (p = 0) and V scale 0
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
-                // V scales of the four tokens of this lane's B fragment (0 past the split end)
                 float sv[4];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
@@ -435,9 +453,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 uint32_t b0[NT], b1[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float *pr = p_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
-                    b0[nt] = pack_f16x2(pr[0] * sv[0], pr[C::PS] * sv[1]);
-                    b1[nt] = pack_f16x2(pr[8 * C::PS] * sv[2], pr[9 * C::PS] * sv[3]);
+                    const float *sr = s_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
+                    const float p0 = ex2(sr[0] - msub[nt]), p1 = ex2(sr[C::PS] - msub[nt]);
+                    const float p2 = ex2(sr[8 * C::PS] - msub[nt]), p3 = ex2(sr[9 * C::PS] - msub[nt]);
+                    lg[nt] += (p0 + p1) + (p2 + p3);
+                    b0[nt] = pack_f16x2(p0 * sv[0], p1 * sv[1]);
+                    b1[nt] = pack_f16x2(p2 * sv[2], p3 * sv[3]);
                 }
 #pragma unroll
                 for (int t = 0; t < MTW; ++t) {
@@ -453,44 +474,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 }
             }
         }
-        // release the stage; the last warp to release it refills it with tile j + kS
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(bar_empty + 8 * st);
-            if (atomicAdd(&s_rel[st], 1) == kW - 1) {
-                s_rel[st] = 0;
-                const int jn = j + kS;
-                if (jn < n_tiles && !s_timeout) {
-                    // completes at once (this was the stage's last release) and orders
-                    // the other warps' reads of the stage before the refill
-                    if (mbar_wait(bar_empty + 8 * st, (j / kS) & 1)) {
-                        issue_tile<C, KG, VG>(base, bar_full + 8 * st, &tmk, &tmv, ksc, vsc,
-                                              plane_row + lo + jn * kTile);
-                        atomicMax(&s_issued, jn + 1);
-                    } else {
-                        s_timeout = 1;
-                    }
-                }
-            }
-        }
     }
+    // the dependent launch (the merge of the splits) may start now: its CTAs
+    // find the SMs that finishing CTAs of this grid leave free
+    pdl_trigger();
 
-    // ---- row sums over the CTA, then each warp writes its head_dim slice ----
+    // row sums: each lane summed a quarter of the tokens of its fragment row
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
-            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
-        }
-    if (gid == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            red_l[warp * 32 + nt * 8 + 2 * tig] = l[nt][0];
-            red_l[warp * 32 + nt * 8 + 2 * tig + 1] = l[nt][1];
-        }
+    for (int nt = 0; nt < NT; ++nt) {
+        lg[nt] += __shfl_xor_sync(0xffffffffu, lg[nt], 1);
+        lg[nt] += __shfl_xor_sync(0xffffffffu, lg[nt], 2);
     }
-    __syncthreads();
     // never leave while a copy into this CTA's shared memory could be in flight
     // (only possible after a timeout; otherwise every issued copy was waited on)
     if (threadIdx.x == 0 && s_timeout) {
@@ -503,12 +497,12 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+            // accumulator column 2 tig + (c & 1): its sum and maximum sit in the lanes
+            // whose fragment row it is
+            const float L = __shfl_sync(0xffffffffu, lg[nt], 8 * tig + 4 * (c & 1));
+            const float M = __shfl_sync(0xffffffffu, mg[nt], 8 * tig + 4 * (c & 1));
             const int n = nt * 8 + 2 * tig + (c & 1);
             if (n >= R) continue;
-            float L = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kW; ++w) L += red_l[w * 32 + n];
-            const float M = m[nt][c & 1];
             const bool empty = (M == -INFINITY || L <= 0.0f);
             const float inv = empty ? 0.0f : 1.0f / L;
             const int i = n / G, jj = n % G;

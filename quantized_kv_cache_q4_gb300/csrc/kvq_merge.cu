@@ -115,10 +115,10 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
 {
     if (rows == 0) return cudaSuccess;
     const dim3 grid((unsigned)rows, (unsigned)ceil_div(head_dim / 4, kMergeCols));
-    // a plain launch: launched early (programmatically) its CTAs would crowd onto
-    // the few SMs the decode kernel leaves free and run far slower
-    merge_kernel<<<grid, kMergeThreads, 0, st>>>(po, pl, n_splits, rows, head_dim, out, out_lse);
-    return cudaGetLastError();
+    // programmatic launch: the decode kernel releases it only after its main
+    // loop, so its CTAs are placed on SMs that finishing decode CTAs free, and
+    // the launch latency hides behind the decode's tail
+    return launch_pdl(merge_kernel, grid, dim3(kMergeThreads), 0, st, po, pl, n_splits, rows, head_dim, out, out_lse);
 }
 
 }  // namespace kvq
