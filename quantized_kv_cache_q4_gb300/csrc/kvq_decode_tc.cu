@@ -27,8 +27,9 @@
 //    O^T += V^T P'^T for its quarter of head_dim over the tile's 64 tokens:
 //    V^T fragments from ldmatrix.trans (it pairs two tokens at one head_dim
 //    index, the A-fragment pairing), V codes again with their fp16 bias, which
-//    a second MMA against a constant operand removes after every 16 tokens;
-//    P' = p * v_scale(token) is rounded once to fp16.
+//    is removed once per tile from the tile's sum of P' (one MMA against a
+//    ones operand per 16 tokens); P' = p * v_scale(token) is rounded once to
+//    fp16.
 //  * Because the warps share the maximum and each owns its own columns, the
 //    end of the CTA is a division by the row sum: no cross-warp combine.
 //
@@ -266,6 +267,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     }
     const uint32_t voff0 = VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), 2 * g_w + ((lane >> 3) & 1));
     const uint32_t qp_base = smem_u32(qp);
+    // with one n-tile the query's B fragments fit in registers for the whole CTA
+    constexpr bool QREG = (NT == 1);
+    constexpr int KSTEPS = D / 16;
+    uint32_t qf[QREG ? KSTEPS : 1][2];
+    if constexpr (QREG) {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+            ldsm_x2(qp_base + qp_chunk_off<D>(lane & 7, 2 * ks + ((lane >> 3) & 1)), qf[ks][0], qf[ks][1]);
+    }
 
     float o[MTW][NT][4];
 #pragma unroll
@@ -339,7 +349,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                         // B fragments of n-tiles 2np and 2np+1 (the second exists only
                         // when 2np + 1 < NT)
                         uint32_t b00, b01, b10, b11;
-                        if (2 * np + 1 < NT) {
+                        if constexpr (QREG) {
+                            b00 = qf[ks][0];
+                            b01 = qf[ks][1];
+                            b10 = b11 = 0u;
+                        } else if (2 * np + 1 < NT) {
                             const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
                             ldsm_x4(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
                         } else {
@@ -438,6 +452,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             float msub[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
+            // sum over the tile's tokens of P' per row (the same in all 16 accumulator
+            // rows), for removing the codes' fp16 bias once per tile
+            float psum[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) psum[nt][c] = 0.0f;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
                 // tokens past the split end have score -inf (p = 0) and V scale 0
@@ -460,18 +481,26 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                     b0[nt] = pack_f16x2(p0 * sv[0], p1 * sv[1]);
                     b1[nt] = pack_f16x2(p2 * sv[2], p3 * sv[3]);
                 }
+                constexpr uint32_t kOnes = 0x3C003C00u;                 // fp16x2 (1, 1)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(psum[nt], kOnes, kOnes, kOnes, kOnes, b0[nt], b1[nt]);
 #pragma unroll
                 for (int t = 0; t < MTW; ++t) {
                     const int e = e0 + t;
                     const uint32_t a0 = q4_pair_biased(r0, e), a1 = q4_pair_biased(r1, e);
                     const uint32_t a2 = q4_pair_biased(r2, e), a3 = q4_pair_biased(r3, e);
-                    const uint32_t nb = (e & 1) ? 0xE480E480u : 0xE408E408u;   // fp16x2 -1152 / -1032
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma16816(o[t][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
-                        mma16816(o[t][nt], nb, nb, nb, nb, b0[nt], b1[nt]);
-                    }
+                    for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
                 }
+            }
+            // remove the bias: 1032 per P' for even nibble pairs, 1152 for odd ones
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+                const float cb = ((e0 + t) & 1) ? -1152.0f : -1032.0f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) o[t][nt][c] = fmaf(cb, psum[nt][c], o[t][nt][c]);
             }
         }
     }
