@@ -115,6 +115,52 @@ __device__ __forceinline__ uint32_t q4_pair_biased(uint32_t w, int e)
     return (e & 1) ? lop3_ac(x, 0x64806480u, 0x64706470u) : lop3_ac(x, 0x64086408u, 0x64076407u);
 }
 
+// The query rows as fp16, head_dim permuted to the K-unpack order and swizzled
+// for ldmatrix ([ROWS][D], rows >= R zero); with Q4_G64 K the odd head_dim
+// indices are divided by 16 (exact for normal values) because their codes
+// arrive as 1152 + 16 q.  Each thread builds whole 16-byte chunks (8
+// k-positions of one k-step, so of one K group); the CPG chunks of a group sit
+// in consecutive lanes, whose shuffle sum gives minus the group's bias term
+// sum_d bias(d) q(d) (bias 1032 at even, 1152 at odd d for Q4_G64; 1152 for
+// q8_0) in kb_s[group][row].
+template <int KC, int D, int ROWS, typename QT>
+__device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb_s, int R, bool ok)
+{
+    constexpr int CPR = D / 8;                     // chunks per row
+    constexpr int CPG = group_size(KC) / 8;        // chunks per K group
+    for (int ci = threadIdx.x; ci < ROWS * CPR; ci += kT) {    // whole warps per step
+        const int n = ci / CPR, c = ci % CPR;
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int kg = 8 * c + j;
+            const int d = kpos_to_d<KC>(kg >> 4, kg & 15);
+            x[j] = 0.0f;
+            if (n < R && ok) {
+                if constexpr (sizeof(QT) == 2) x[j] = __half2float(qst[n * D + d]);
+                else x[j] = __half2float(__float2half_rn(qst[n * D + d]));
+            }
+            if constexpr (KC == KVQ_CODEC_Q4_G64)
+                if (d & 1) x[j] *= 0.0625f;
+        }
+        uint32_t hw[4];
+        float b = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hw[j] = pack_f16x2(x[2 * j], x[2 * j + 1]);
+            const float2 hf = __half22float2(u32_as_h2(hw[j]));
+            // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
+            const int kg = 8 * c + 2 * j;
+            const bool even = (KC == KVQ_CODEC_Q4_G64) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
+            b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
+        }
+        *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+#pragma unroll
+        for (int off = 1; off < CPG; off <<= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
+        if (c % CPG == 0) kb_s[(c / CPG) * ROWS + n] = -b;
+    }
+}
+
 template <typename C, typename KG, typename VG>
 __device__ __forceinline__ void issue_tile(uint32_t base, uint32_t full, const CUtensorMap *tmk,
                                            const CUtensorMap *tmv, const uint8_t *ksc, const uint8_t *vsc,
@@ -198,51 +244,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         s_issued = first;
     }
 
-    // The query as fp16, head_dim permuted to the K-unpack order and swizzled for
-    // ldmatrix; with Q4_G64 K the odd head_dim indices are divided by 16 (exact
-    // for normal values) because their codes arrive as 1152 + 16 q.  Each thread
-    // builds whole 16-byte chunks (8 k-positions of one k-step, so of one K
-    // group); the CPG chunks of a group sit in consecutive lanes, whose shuffle
-    // sum gives the group's bias term sum_d bias(d) q(d) (bias 1032 at even,
-    // 1152 at odd d for Q4_G64; 1152 for q8_0).
+    // the query rows, permuted and swizzled, and the K bias terms
     if (!mbar_wait(bar_q, 0)) s_timeout = 1;
-    {
-        constexpr int CPR = D / 8;                     // chunks per row
-        constexpr int CPG = group_size(KC) / 8;        // chunks per K group
-        const QT *qst = reinterpret_cast<const QT *>(smem + C::QST_OFF);
-        const bool ok = !s_timeout;
-        for (int ci = threadIdx.x; ci < C::ROWS * CPR; ci += kT) {    // whole warps per step
-            const int n = ci / CPR, c = ci % CPR;
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int kg = 8 * c + j;
-                const int d = kpos_to_d<KC>(kg >> 4, kg & 15);
-                x[j] = 0.0f;
-                if (n < R && ok) {
-                    if constexpr (sizeof(QT) == 2) x[j] = __half2float(qst[n * D + d]);
-                    else x[j] = __half2float(__float2half_rn(qst[n * D + d]));
-                }
-                if constexpr (KC == KVQ_CODEC_Q4_G64)
-                    if (d & 1) x[j] *= 0.0625f;
-            }
-            uint32_t hw[4];
-            float b = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                hw[j] = pack_f16x2(x[2 * j], x[2 * j + 1]);
-                const float2 hf = __half22float2(u32_as_h2(hw[j]));
-                // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
-                const int kg = 8 * c + 2 * j;
-                const bool even = (KC == KVQ_CODEC_Q4_G64) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
-                b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
-            }
-            *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-#pragma unroll
-            for (int off = 1; off < CPG; off <<= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
-            if (c % CPG == 0) kb_s[(c / CPG) * C::ROWS + n] = -b;
-        }
-    }
+    prep_query<KC, D, C::ROWS>(reinterpret_cast<const QT *>(smem + C::QST_OFF), qp, kb_s, R, !s_timeout);
     __syncthreads();
 
     int nv[NT][2];
@@ -563,16 +567,14 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int KC, int D, int NT, typename QT>
-cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
+template <typename C, typename Kern>
+cudaError_t launch_cfg(Kern kern, const DecodeArgs &a, cudaStream_t st)
 {
-    using C = TcCfg<KC, D, NT, QT>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory of one CTA");
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
     CUtensorMap tk, tv;
     if (!make_codes_map(&tk, a.k.qs, C::KRB, rows) || !make_codes_map(&tv, a.v.qs, C::VRB, rows))
         return cudaErrorInvalidValue;
-    auto kern = decode_tc_kernel<KC, D, NT, QT>;
     static bool attr_set[64] = {};           // the attributes are per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -587,6 +589,12 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
     }
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
     return launch_pdl(kern, grid, dim3(kT), C::SMEM, st, a, tk, tv);
+}
+
+template <int KC, int D, int NT, typename QT>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
+{
+    return launch_cfg<TcCfg<KC, D, NT, QT>>(decode_tc_kernel<KC, D, NT, QT>, a, st);
 }
 
 template <int KC, int D, typename QT>

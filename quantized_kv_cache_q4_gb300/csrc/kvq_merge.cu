@@ -5,81 +5,60 @@
 // out = sum_s w_s o_s / sum_s w_s and lse = M + ln sum_s w_s.  Parts with
 // lse = -inf (no visible key) carry no weight and their o is never used.
 //
-// The merge is latency-bound (a few KB per row, straight after the decode
-// kernel wrote them), so it is laid out for one round of loads: a block of
-// 256 threads covers 16 float4 columns of one row, 16 threads per column, and
-// thread j of a column reads the lse and the float4 of splits j, j+16, ...
-// together, keeping a running maximum.  The 16 lanes of a column then combine
-// their (maximum, weight sum, weighted sum) with shuffles; there is no block
-// barrier.
+// The merge is latency-bound (the partials were just written, so they sit in
+// L2): it is laid out for at most a round or two of loads per thread.  LPC
+// consecutive lanes own one float4 column of one row; lane j of the group reads
+// the lse and the float4 of splits j, j + LPC, ... four at a time (all issued
+// before any is used), keeping a running maximum, and the group combines its
+// (maximum, weight sum, weighted sum) with shuffles.  LPC grows with the split
+// count (many splits: a warp per column; few splits, many rows: a lane per
+// column) so that both shapes need few rounds and few CTAs.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kLanesPerCol = 16;                          // split lanes per float4 column
-constexpr int kMergeCols = kMergeThreads / kLanesPerCol;  // float4 columns per block
 constexpr int kUnroll = 4;
 
-__device__ __forceinline__ float group_max(float x)
-{
-#pragma unroll
-    for (int o = 1; o < kLanesPerCol; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
-
-__device__ __forceinline__ float group_sum(float x)
-{
-#pragma unroll
-    for (int o = 1; o < kLanesPerCol; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
+template <int LPC>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_splits, int rows, int D,
              float *__restrict__ out, float *__restrict__ out_lse)
 {
-    const int row = blockIdx.x;
-    const int sl = threadIdx.x % kLanesPerCol;
-    const int col = blockIdx.y * kMergeCols + threadIdx.x / kLanesPerCol;   // float4 column
     const int D4 = D / 4;
-    const bool has_col = col < D4;
+    const int sl = threadIdx.x % LPC;
+    const int64_t item = (int64_t)blockIdx.x * (kMergeThreads / LPC) + threadIdx.x / LPC;
+    const bool active = item < (int64_t)rows * D4;     // idle groups still take part in the shuffles
+    const int row = active ? (int)(item / D4) : 0, col = active ? (int)(item % D4) : 0;
     pdl_wait();
     pdl_trigger();
 
-    // one pass over this lane's splits, loading lse and values together and
-    // keeping a running maximum (weights relative to it, rescaled when it grows)
     float M = -INFINITY, W = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = sl; s0 < n_splits; s0 += kLanesPerCol * kUnroll) {
+    for (int s0 = sl; active && s0 < n_splits; s0 += LPC * kUnroll) {
         float l[kUnroll];
         float4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int s = s0 + u * kLanesPerCol;
+            const int s = s0 + u * LPC;
             l[u] = (s < n_splits) ? pl[(int64_t)s * rows + row] : -INFINITY;
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int s = s0 + u * kLanesPerCol;
             // loaded whether or not the part is empty (independent of the lse load);
             // an empty part's values are never used below
-            v[u] = (s < n_splits && has_col)
-                       ? reinterpret_cast<const float4 *>(po + ((int64_t)s * rows + row) * D)[col]
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = (s < n_splits) ? reinterpret_cast<const float4 *>(po + ((int64_t)s * rows + row) * D)[col]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mu = M;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) mu = fmaxf(mu, l[u]);
-        if (mu == -INFINITY) continue;                 // nothing but empty parts so far
-        const float r = expf(M - mu);                  // 0 when M is still -inf
+        if (mu == -INFINITY) continue;         // nothing but empty parts so far
+        const float r = expf(M - mu);          // 0 when M is still -inf
         W *= r;
         acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
         M = mu;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            if (l[u] == -INFINITY) continue;          // empty part: no weight, value never used
+            if (l[u] == -INFINITY) continue;  // empty part: no weight, value never used
             const float w = expf(l[u] - M);
             W += w;
             acc.x = fmaf(w, v[u].x, acc.x);
@@ -88,24 +67,42 @@ merge_kernel(const float *__restrict__ po, const float *__restrict__ pl, int n_s
             acc.w = fmaf(w, v[u].w, acc.w);
         }
     }
-    // combine the 16 lanes of the column: common maximum, rescaled sums
-    const float Mg = group_max(M);
+    // combine the LPC lanes of the column: common maximum, rescaled sums
+    float Mg = M;
+#pragma unroll
+    for (int o = LPC / 2; o > 0; o >>= 1) Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
     const float r = (M == -INFINITY) ? 0.0f : expf(M - Mg);
-    W = group_sum(W * r);
-    acc.x = group_sum(acc.x * r);
-    acc.y = group_sum(acc.y * r);
-    acc.z = group_sum(acc.z * r);
-    acc.w = group_sum(acc.w * r);
-    M = Mg;
-    if (sl == 0 && has_col) {
+    W *= r;
+    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+    for (int o = LPC / 2; o > 0; o >>= 1) {
+        W += __shfl_xor_sync(0xffffffffu, W, o);
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    if (active && sl == 0) {
         float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
+        if (Mg != -INFINITY) {
             const float inv = 1.0f / W;
             res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
         reinterpret_cast<float4 *>(out + (int64_t)row * D)[col] = res;
-        if (col == 0 && out_lse) out_lse[row] = (M == -INFINITY) ? -INFINITY : M + logf(W);
+        if (col == 0 && out_lse) out_lse[row] = (Mg == -INFINITY) ? -INFINITY : Mg + logf(W);
     }
+}
+
+template <int LPC>
+cudaError_t launch_lpc(const float *po, const float *pl, int n_splits, int rows, int D, float *out, float *out_lse,
+                       cudaStream_t st)
+{
+    const int64_t items = (int64_t)rows * (D / 4);
+    const dim3 grid((unsigned)ceil_div(items, kMergeThreads / LPC));
+    // programmatic launch: the decode kernel releases it only after its main
+    // loop, so its CTAs are placed on SMs that finishing decode CTAs free, and
+    // the launch latency hides behind the decode's tail
+    return launch_pdl(merge_kernel<LPC>, grid, dim3(kMergeThreads), 0, st, po, pl, n_splits, rows, D, out, out_lse);
 }
 
 }  // namespace
@@ -114,11 +111,20 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
                          float *out, float *out_lse, cudaStream_t st)
 {
     if (rows == 0) return cudaSuccess;
-    const dim3 grid((unsigned)rows, (unsigned)ceil_div(head_dim / 4, kMergeCols));
-    // programmatic launch: the decode kernel releases it only after its main
-    // loop, so its CTAs are placed on SMs that finishing decode CTAs free, and
-    // the launch latency hides behind the decode's tail
-    return launch_pdl(merge_kernel, grid, dim3(kMergeThreads), 0, st, po, pl, n_splits, rows, head_dim, out, out_lse);
+    // lanes per column: enough that a lane loads at most kUnroll splits, fewer
+    // while that would take more than about two waves of threads
+    int lpc = 1;
+    while (lpc < 32 && lpc * kUnroll < n_splits) lpc *= 2;
+    const int64_t items = (int64_t)rows * (head_dim / 4);
+    while (lpc > 1 && items * lpc > 2LL * 152 * 2048) lpc /= 2;
+    switch (lpc) {
+    case 1: return launch_lpc<1>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    case 2: return launch_lpc<2>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    case 4: return launch_lpc<4>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    case 8: return launch_lpc<8>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    case 16: return launch_lpc<16>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    default: return launch_lpc<32>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
+    }
 }
 
 }  // namespace kvq

@@ -105,3 +105,25 @@ def test_equal_scores_mean_of_v_on_gpu():
     Vh = oracle.dequantize(vo.codec, vo.qs[0, 0, :4096], vo.scales[0, 0, :4096], 256).astype(np.float64)
     assert np.abs(o[0, 0] - Vh.mean(axis=0)[None]).max() < 1e-4
     assert np.abs(lse - np.log(4096)).max() < 1e-4
+
+
+@pytest.mark.parametrize("n_splits", [0, 16, 1024])
+def test_workspace_reused_across_calls(n_splits):
+    """One workspace serves call after call (its contents are scratch that no
+    call relies on), including split counts with many empty splits."""
+    wl = workloads.custom(n_seq=1, n_heads=24, n_kv_heads=4, head_dim=256, cached=(4095,), n_new=1,
+                          src_dtype="f16", q_dtype="f16", dist="outliers", seed=51)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    S, nq, H, D = wl.q.shape
+    max_kv = int(wl.kv_len.max())
+    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(S, 4, H, nq, D, max_kv, n_splits))
+    for _ in range(3):
+        out = torch.full((S, nq, H, D), float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full((S, nq, H), float("nan"), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvq.kvq_decode_attention(k, v, dev(wl.q), nq, H, wl.spec.scale, dev(wl.kv_len), max_kv, n_splits, out, lse,
+                                 ws, d_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        check_close(out.cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref)
