@@ -249,8 +249,8 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
     pos0, kv_len = to_dev(wl.cached_len), to_dev(wl.kv_len)
     max_kv = int(wl.kv_len.max())
     n_splits = args.splits if args.splits is not None else 0
-    n_splits_eff = n_splits or kvq.kvq_decode_default_splits(S, Hk, H, nq, D, max_kv)
-    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(S, Hk, H, nq, D, max_kv, n_splits), dev)
+    n_splits_eff = n_splits or kvq.kvq_decode_default_splits(k0, v0, H, nq, max_kv)
+    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(k0, v0, H, nq, max_kv, n_splits), dev)
     out = torch.empty((S, nq, H, D), dtype=torch.float32, device=dev)
     lse = torch.empty((S, nq, H), dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -113,15 +113,21 @@ kvq_status kvq_quantize_append(const kvq_cache *k, const kvq_cache *v,
                                int32_t n_new, const int32_t *d_pos0, int32_t *d_err,
                                void *stream);
 
-/* Split count the library uses for kvq_decode_attention(n_splits = 0) on the
- * current device: enough (sequence, kv head, split) work items to fill the GPU. */
-int32_t kvq_decode_default_splits(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
-                                  int32_t head_dim, int32_t max_kv_len);
+/* Split count kvq_decode_attention uses for n_splits = 0 with these caches and
+ * arguments on the current device.  One sequence: one wave of the decode
+ * kernel's CTAs (how many fit on an SM depends on the K codec, head_dim and the
+ * query rows per kv head); a batch, whose lengths may be ragged: up to four
+ * waves' worth at three CTAs per SM.  Never fewer than 256 keys per split.
+ * Only codec, n_seq, n_kv_heads and head_dim of k and v are read (their plane
+ * pointers may be NULL).  Returns 1 for invalid arguments. */
+int32_t kvq_decode_default_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
+                                  int32_t max_kv_len);
 
-/* Device workspace bytes kvq_decode_attention needs for these arguments
- * (n_splits as passed to it, 0 = the default).  0 means none is needed. */
-size_t kvq_decode_workspace_bytes(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
-                                  int32_t head_dim, int32_t max_kv_len, int32_t n_splits);
+/* Device workspace bytes kvq_decode_attention needs for these caches and
+ * arguments (n_splits as passed to it, 0 = the default).  0 means none is
+ * needed (also returned for invalid arguments). */
+size_t kvq_decode_workspace_bytes(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
+                                  int32_t max_kv_len, int32_t n_splits);
 
 /* Decode / MTP-verify attention over the packed cache (the attention stage).
  *   k, v          : caches with the same n_seq, n_kv_heads, head_dim, capacity.

@@ -48,8 +48,8 @@ def _load():
         "kvq_row_bytes": (I32, [I32, I32]),
         "kvq_scales_per_row": (I32, [I32, I32]),
         "kvq_quantize_append": (I32, [C, C, P, P, I32, I32, P, P, P]),
-        "kvq_decode_default_splits": (I32, [I32, I32, I32, I32, I32, I32]),
-        "kvq_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
+        "kvq_decode_default_splits": (I32, [C, C, I32, I32, I32]),
+        "kvq_decode_workspace_bytes": (SZ, [C, C, I32, I32, I32, I32]),
         "kvq_decode_attention": (I32, [C, C, P, I32, I32, I32, F, P, I32, I32, P, P, P, SZ, P, P]),
         "kvq_merge_splits": (I32, [P, P, I32, I32, I32, P, P, P]),
         "kvq_dequantize": (I32, [C, P, P]),
@@ -149,12 +149,18 @@ def kvq_quantize_append(k: KVCache | None, v: KVCache | None, k_src, v_src, n_ne
                                     _ptr(d_err), _stream(stream)))
 
 
-def kvq_decode_default_splits(n_seq, n_kv_heads, n_heads, n_q, head_dim, max_kv_len) -> int:
-    return int(_lib.kvq_decode_default_splits(n_seq, n_kv_heads, n_heads, n_q, head_dim, max_kv_len))
+def _cref(c):
+    """A KVCache or a bare kvq_cache structure, as the C pointer argument."""
+    return c.c if isinstance(c, KVCache) else ctypes.byref(c)
 
 
-def kvq_decode_workspace_bytes(n_seq, n_kv_heads, n_heads, n_q, head_dim, max_kv_len, n_splits=0) -> int:
-    return int(_lib.kvq_decode_workspace_bytes(n_seq, n_kv_heads, n_heads, n_q, head_dim, max_kv_len, n_splits))
+def kvq_decode_default_splits(k, v, n_heads: int, n_q: int, max_kv_len: int) -> int:
+    return int(_lib.kvq_decode_default_splits(_cref(k), _cref(v), int(n_heads), int(n_q), int(max_kv_len)))
+
+
+def kvq_decode_workspace_bytes(k, v, n_heads: int, n_q: int, max_kv_len: int, n_splits: int = 0) -> int:
+    return int(_lib.kvq_decode_workspace_bytes(_cref(k), _cref(v), int(n_heads), int(n_q), int(max_kv_len),
+                                               int(n_splits)))
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor | None:
@@ -218,8 +224,7 @@ def decode(k: KVCache, v: KVCache, q: torch.Tensor, d_kv_len: torch.Tensor, max_
         softmax_scale = D ** -0.5
     out = torch.empty((n_seq, n_q, n_heads, D), dtype=torch.float32, device=q.device)
     lse = torch.empty((n_seq, n_q, n_heads), dtype=torch.float32, device=q.device)
-    ws = alloc_workspace(kvq_decode_workspace_bytes(n_seq, k.n_kv_heads, n_heads, n_q, D, max_kv_len, n_splits),
-                         q.device)
+    ws = alloc_workspace(kvq_decode_workspace_bytes(k, v, n_heads, n_q, max_kv_len, n_splits), q.device)
     kvq_decode_attention(k, v, q, n_q, n_heads, softmax_scale, d_kv_len, max_kv_len, n_splits, out, lse, ws,
                          d_err=d_err, stream=stream)
     return out, lse

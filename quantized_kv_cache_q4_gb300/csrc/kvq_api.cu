@@ -70,15 +70,31 @@ int sm_count()
 
 constexpr int kMaxSplits = 4096;
 
-int resolve_splits(int32_t n_seq, int32_t n_kv_heads, int32_t max_kv_len, int32_t n_splits)
+bool split_args_ok(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q, int32_t max_kv_len)
+{
+    return k && v && k->n_seq > 0 && k->n_kv_heads > 0 && k->head_dim > 0 && n_heads > 0 && n_q > 0 &&
+           n_heads % k->n_kv_heads == 0 && max_kv_len > 0;
+}
+
+// Arguments the split policy reads are valid (checked by every caller).
+int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q, int32_t max_kv_len,
+                   int32_t n_splits)
 {
     if (n_splits > 0) return n_splits;
-    const int64_t units = (int64_t)n_seq * n_kv_heads;
-    // one wave of CTAs (3 per SM) for a single sequence; for a batch, whose
-    // lengths may be ragged, up to four waves so that the longest sequence is
-    // cut finely enough (every sequence gets the same number of splits)
-    const int64_t waves = n_seq < 4 ? n_seq : 4;
-    const int64_t target = 3LL * sm_count() * waves;
+    const int64_t units = (int64_t)k->n_seq * k->n_kv_heads;
+    int64_t target;
+    if (k->n_seq == 1) {
+        // one wave of the decode kernel's CTAs
+        int per_sm = kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, n_q * (n_heads / k->n_kv_heads));
+        if (per_sm <= 0) per_sm = 3;
+        target = (int64_t)per_sm * sm_count();
+    } else {
+        // a batch, whose lengths may be ragged: up to four waves at 3 CTAs per SM
+        // so that the longest sequence is cut finely enough (every sequence gets
+        // the same number of splits)
+        const int64_t waves = k->n_seq < 4 ? k->n_seq : 4;
+        target = 3LL * sm_count() * waves;
+    }
     int64_t s = kvq::ceil_div(target, units);
     const int64_t max_useful = kvq::ceil_div(max_kv_len, 256);      // at least 256 tokens a split
     if (s > max_useful) s = max_useful;
@@ -161,24 +177,21 @@ kvq_status kvq_quantize_append(const kvq_cache *k, const kvq_cache *v, const voi
                        "append launch");
 }
 
-int32_t kvq_decode_default_splits(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
-                                  int32_t head_dim, int32_t max_kv_len)
+int32_t kvq_decode_default_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
+                                  int32_t max_kv_len)
 {
-    (void)n_heads; (void)n_q; (void)head_dim;
-    if (n_seq <= 0 || n_kv_heads <= 0 || max_kv_len <= 0) return 1;
-    return resolve_splits(n_seq, n_kv_heads, max_kv_len, 0);
+    if (!split_args_ok(k, v, n_heads, n_q, max_kv_len)) return 1;
+    return resolve_splits(k, v, n_heads, n_q, max_kv_len, 0);
 }
 
-size_t kvq_decode_workspace_bytes(int32_t n_seq, int32_t n_kv_heads, int32_t n_heads, int32_t n_q,
-                                  int32_t head_dim, int32_t max_kv_len, int32_t n_splits)
+size_t kvq_decode_workspace_bytes(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
+                                  int32_t max_kv_len, int32_t n_splits)
 {
-    if (n_seq <= 0 || n_kv_heads <= 0 || n_heads <= 0 || n_q <= 0 || head_dim <= 0 || max_kv_len <= 0 ||
-        n_splits < 0)
-        return 0;
-    const int s = resolve_splits(n_seq, n_kv_heads, max_kv_len, n_splits);
+    if (!split_args_ok(k, v, n_heads, n_q, max_kv_len) || n_splits < 0) return 0;
+    const int s = resolve_splits(k, v, n_heads, n_q, max_kv_len, n_splits);
     if (s <= 1) return 0;
-    const size_t rows = (size_t)n_seq * n_q * n_heads;
-    return align256((size_t)s * rows * head_dim * sizeof(float)) + align256((size_t)s * rows * sizeof(float));
+    const size_t rows = (size_t)k->n_seq * n_q * n_heads;
+    return align256((size_t)s * rows * k->head_dim * sizeof(float)) + align256((size_t)s * rows * sizeof(float));
 }
 
 kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const void *q, int32_t q_dtype,
@@ -207,9 +220,8 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const vo
     if (n_splits < 0 || n_splits > kMaxSplits)
         return fail(KVQ_EINVAL, "decode: n_splits=%d outside [0, %d]", n_splits, kMaxSplits);
     if (!out) return fail(KVQ_EINVAL, "decode: out is NULL");
-    const int s = resolve_splits(k->n_seq, k->n_kv_heads, max_kv_len, n_splits);
-    const size_t need = kvq_decode_workspace_bytes(k->n_seq, k->n_kv_heads, n_heads, n_q, k->head_dim,
-                                                   max_kv_len, n_splits);
+    const int s = resolve_splits(k, v, n_heads, n_q, max_kv_len, n_splits);
+    const size_t need = kvq_decode_workspace_bytes(k, v, n_heads, n_q, max_kv_len, n_splits);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(KVQ_EWORKSPACE, "decode: workspace %zu bytes given, %zu needed", workspace ? workspace_bytes : 0,
                     need);

@@ -198,7 +198,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     __shared__ volatile int s_timeout;
     __shared__ int s_issued;
 
-    const int split = blockIdx.x, kh = blockIdx.y, s = blockIdx.z;
+    const int split = blockIdx.x, kh = blockIdx.y;
+    __shared__ int s_seq;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int G = a.n_heads / a.n_kv_heads;
@@ -214,6 +215,23 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     }
     __syncthreads();
     pdl_wait();
+    // The grid's z index is a rank: sequences in order of decreasing length, so
+    // the CTAs of the longest sequences of a ragged batch are dispatched first
+    // (a longest-first schedule).  Ties go by index; identity beyond kT sequences.
+    int s = blockIdx.z;
+    if (a.n_seq > 1 && a.n_seq <= kT) {
+        if ((int)threadIdx.x < a.n_seq) {
+            const int t = threadIdx.x, lt = a.kv_len[t];
+            int rank = 0;
+            for (int u = 0; u < a.n_seq; ++u) {
+                const int lu = a.kv_len[u];
+                rank += (lu > lt) || (lu == lt && u < t);
+            }
+            if (rank == (int)blockIdx.z) s_seq = t;
+        }
+        __syncthreads();
+        s = s_seq;
+    }
     // query rows (for each query token, the G heads of this kv head are one
     // contiguous run) by bulk copy, in parallel with what follows
     if (threadIdx.x == 0) {
@@ -567,6 +585,31 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// Kernel attributes (dynamic shared memory, carveout), set once per device, and
+// the CTAs per SM they allow.
+template <typename C, typename Kern>
+cudaError_t prepare_kernel(Kern kern, int *per_sm)
+{
+    static int resident[64] = {};            // per device; 0 = not prepared yet
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && resident[dev] > 0) {
+        *per_sm = resident[dev];
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kT, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) resident[dev] = n;
+    *per_sm = n;
+    return cudaSuccess;
+}
+
 template <typename C, typename Kern>
 cudaError_t launch_cfg(Kern kern, const DecodeArgs &a, cudaStream_t st)
 {
@@ -575,20 +618,41 @@ cudaError_t launch_cfg(Kern kern, const DecodeArgs &a, cudaStream_t st)
     CUtensorMap tk, tv;
     if (!make_codes_map(&tk, a.k.qs, C::KRB, rows) || !make_codes_map(&tv, a.v.qs, C::VRB, rows))
         return cudaErrorInvalidValue;
-    static bool attr_set[64] = {};           // the attributes are per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int per_sm = 0;
+    cudaError_t e = prepare_kernel<C>(kern, &per_sm);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
     return launch_pdl(kern, grid, dim3(kT), C::SMEM, st, a, tk, tv);
+}
+
+template <int KC, int D>
+int per_sm_nt(int nt)
+{
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (nt) {
+    case 1: e = prepare_kernel<TcCfg<KC, D, 1, __half>>(decode_tc_kernel<KC, D, 1, __half>, &n); break;
+    case 2: e = prepare_kernel<TcCfg<KC, D, 2, __half>>(decode_tc_kernel<KC, D, 2, __half>, &n); break;
+    case 3: e = prepare_kernel<TcCfg<KC, D, 3, __half>>(decode_tc_kernel<KC, D, 3, __half>, &n); break;
+    case 4: e = prepare_kernel<TcCfg<KC, D, 4, __half>>(decode_tc_kernel<KC, D, 4, __half>, &n); break;
+    default: break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int KC>
+int per_sm_d(int head_dim, int nt)
+{
+    switch (head_dim) {
+    case 64: return per_sm_nt<KC, 64>(nt);
+    case 128: return per_sm_nt<KC, 128>(nt);
+    case 256: return per_sm_nt<KC, 256>(nt);
+    default: return 0;
+    }
 }
 
 template <int KC, int D, int NT, typename QT>
@@ -630,6 +694,15 @@ bool decode_tc_supported(const DecodeArgs &a)
     return R >= 1 && R <= 32 && a.v.codec == KVQ_CODEC_Q4_G64 &&
            (a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256) && rows < (1LL << 31) &&
            tensor_maps_available();
+}
+
+int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_head)
+{
+    if (v_codec != KVQ_CODEC_Q4_G64 || rows_per_kv_head < 1 || rows_per_kv_head > 32) return 0;
+    const int nt = (rows_per_kv_head + 7) / 8;
+    if (k_codec == KVQ_CODEC_Q4_G64) return per_sm_d<KVQ_CODEC_Q4_G64>(head_dim, nt);
+    if (k_codec == KVQ_CODEC_Q8_0) return per_sm_d<KVQ_CODEC_Q8_0>(head_dim, nt);
+    return 0;
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st)

@@ -39,8 +39,7 @@ kvq_status kvq_decode_attention_static(const kvq_cache *k, const kvq_cache *v, c
 {
     // the scratch this call needs must fit the array; checked before any CUDA call
     if (k && v && n_heads > 0 && n_q > 0 && max_kv_len > 0 && n_splits >= 0) {
-        const size_t need = kvq_decode_workspace_bytes(k->n_seq, k->n_kv_heads, n_heads, n_q, k->head_dim,
-                                                       max_kv_len, n_splits);
+        const size_t need = kvq_decode_workspace_bytes(k, v, n_heads, n_q, max_kv_len, n_splits);
         if (need > (size_t)KVQ_STATIC_SCRATCH_BYTES) {
             char msg[256];
             snprintf(msg, sizeof msg,

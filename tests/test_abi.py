@@ -93,20 +93,26 @@ def test_decode_rejects_bad_arguments():
     assert _decode(k, v, n_splits=5000) == kvq.KVQ_EINVAL
     assert _decode(k, v, out=None) == kvq.KVQ_EINVAL
     assert _decode(k, v, n_splits=8) == kvq.KVQ_EWORKSPACE             # splits need a workspace
-    need = kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 512, 8)
+    need = kvq.kvq_decode_workspace_bytes(k, v, 24, 1, 512, 8)
     assert _decode(k, v, n_splits=8, ws=1 << 20, ws_bytes=need - 1) == kvq.KVQ_EWORKSPACE
     assert _decode(k, v, n_splits=8, ws=(1 << 20) + 16, ws_bytes=need) == kvq.KVQ_EINVAL   # misaligned
 
 
 def test_workspace_sizes():
-    assert kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 32768, 1) == 0
+    k, v = _fake_cache(capacity=32768), _fake_cache(capacity=32768)
+    assert kvq.kvq_decode_workspace_bytes(k, v, 24, 1, 32768, 1) == 0
     rows = 1 * 1 * 24
-    n = kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 32768, 64)
+    n = kvq.kvq_decode_workspace_bytes(k, v, 24, 1, 32768, 64)
     assert n >= 64 * rows * 257 * 4 and n % 256 == 0
-    assert kvq.kvq_decode_workspace_bytes(16, 4, 24, 3, 256, 65539, 16) >= 16 * 16 * 3 * 24 * 257 * 4
-    d = kvq.kvq_decode_default_splits(1, 4, 24, 1, 256, 32768)
+    kb, vb = _fake_cache(n_seq=16, capacity=65600), _fake_cache(n_seq=16, capacity=65600)
+    assert kvq.kvq_decode_workspace_bytes(kb, vb, 24, 3, 65539, 16) >= 16 * 16 * 3 * 24 * 257 * 4
+    d = kvq.kvq_decode_default_splits(k, v, 24, 1, 32768)
     assert 1 <= d <= 4096
-    assert kvq.kvq_decode_default_splits(1, 4, 24, 1, 256, 100) == 1   # short context: no split
+    assert kvq.kvq_decode_workspace_bytes(k, v, 24, 1, 32768) >= d * rows * 257 * 4
+    assert kvq.kvq_decode_default_splits(k, v, 24, 1, 100) == 1        # short context: no split
+    # invalid arguments: one split, no workspace
+    assert kvq.kvq_decode_default_splits(k, v, 22, 1, 32768) == 1      # 22 heads over 4 kv heads
+    assert kvq.kvq_decode_workspace_bytes(k, v, 24, 0, 32768) == 0
 
 
 def test_merge_rejects_bad_arguments():

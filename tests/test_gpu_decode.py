@@ -117,7 +117,7 @@ def test_workspace_reused_across_calls(n_splits):
     o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
     S, nq, H, D = wl.q.shape
     max_kv = int(wl.kv_len.max())
-    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(S, 4, H, nq, D, max_kv, n_splits))
+    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(k, v, H, nq, max_kv, n_splits))
     for _ in range(3):
         out = torch.full((S, nq, H, D), float("nan"), dtype=torch.float32, device="cuda")
         lse = torch.full((S, nq, H), float("nan"), dtype=torch.float32, device="cuda")

@@ -27,7 +27,7 @@ def test_static_scratch_matches_workspace_entry_point_two_calls(n_new, n_splits)
     q, kv_len = dev(wl.q), dev(wl.kv_len)
     max_kv = int(wl.kv_len.max())
     S, nq, H, D = wl.q.shape
-    assert kvq.kvq_decode_workspace_bytes(S, 4, H, nq, D, max_kv, n_splits) <= kvq.kvq_static_scratch_bytes()
+    assert kvq.kvq_decode_workspace_bytes(k, v, H, nq, max_kv, n_splits) <= kvq.kvq_static_scratch_bytes()
     ref, ref_lse = kvq.decode(k, v, q, kv_len, max_kv, wl.spec.scale, n_splits=n_splits)
     for _ in range(2):                         # the array keeps the last call's contents
         out = torch.full((S, nq, H, D), float("nan"), dtype=torch.float32, device="cuda")
@@ -44,7 +44,7 @@ def test_static_scratch_rejects_oversized_request():
                           src_dtype="f16", q_dtype="f16", seed=95)
     k, v = gpu_caches(wl)
     n_splits = 4096
-    need = kvq.kvq_decode_workspace_bytes(1, 4, 24, 1, 256, 2048, n_splits)
+    need = kvq.kvq_decode_workspace_bytes(k, v, 24, 1, 2048, n_splits)
     assert need > kvq.kvq_static_scratch_bytes()
     out = torch.zeros((1, 1, 24, 256), dtype=torch.float32, device="cuda")
     with pytest.raises(kvq.KvqError) as e:
