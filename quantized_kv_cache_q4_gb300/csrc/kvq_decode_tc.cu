@@ -67,8 +67,11 @@ struct TcCfg {
     static constexpr int QST_OFF = U_OFF;
     static constexpr int S_OFF = U_OFF;                                   // fp32 [2][64][PS] scores
     static constexpr int RED_OFF = S_OFF + align_up(2 * kTile * PS * 4, 16);  // fp32 [2][kW][32] maxima
+    // V scales of the tile transposed to [group][token] (0 past the split end), by tile parity
+    static constexpr int NGV = D / 64;
+    static constexpr int VT_OFF = RED_OFF + 2 * kW * 32 * 4;                  // fp16 [2][NGV][64]
     static constexpr int QST_BYTES = ROWS * D * (int)sizeof(QT);
-    static constexpr int PR_BYTES = (RED_OFF - U_OFF) + 2 * kW * 32 * 4;
+    static constexpr int PR_BYTES = (VT_OFF - U_OFF) + 2 * NGV * kTile * 2;
     static constexpr int BAR_OFF = align_up(U_OFF + (QST_BYTES > PR_BYTES ? QST_BYTES : PR_BYTES), 16);
     static constexpr int SMEM = BAR_OFF + (kS + 1) * 8 + 1024;            // + alignment slack
     static constexpr int MTW = (D / 64 * 4) / kW;                 // 16-row head_dim tiles per warp in phase B
@@ -193,6 +196,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     float *kb_s = reinterpret_cast<float *>(smem + C::KB_OFF);
     float *s_s0 = reinterpret_cast<float *>(smem + C::S_OFF);        // [2][64][PS]
     float *red_m0 = reinterpret_cast<float *>(smem + C::RED_OFF);    // [2][kW][32]
+    __half *vt0 = reinterpret_cast<__half *>(smem + C::VT_OFF);      // [2][NGV][64]
     const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);
     const uint32_t bar_q = bar_full + kS * 8;
     __shared__ volatile int s_timeout;
@@ -325,6 +329,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         const uint8_t *vsp = smem + st * C::STAGE + C::VS_OFF;
         float *s_s = s_s0 + (j & 1) * (kTile * C::PS);
         float *red_m = red_m0 + (j & 1) * (kW * 32);
+        __half *vt = vt0 + (j & 1) * (C::NGV * kTile);
+        // this warp's 16 tokens' V scales, transposed for phase B (0 past the split end)
+        for (int i = lane; i < 16 * C::NGV; i += 32) {
+            const int t = i & 15, g = i >> 4;
+            vt[g * kTile + tl + t] =
+                (tb + t < hi) ? reinterpret_cast<const __half *>(vsp + (tl + t) * C::VSB)[g] : __float2half_rn(0.0f);
+        }
 
         // ---- phase A: S^T for this warp's 16 tokens ----
         float sc[NT][4];
@@ -353,16 +364,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                     unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
                     unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
                 }
-                // each group's accumulator starts at minus its bias term
+                // each group's accumulator starts at minus its bias term (the first
+                // k-step's MMA takes it as its accumulator input)
                 float cg[NT][4];
+                float2 nb2[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float2 nb2 = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
-                    cg[nt][0] = nb2.x;
-                    cg[nt][1] = nb2.y;
-                    cg[nt][2] = nb2.x;
-                    cg[nt][3] = nb2.y;
-                }
+                for (int nt = 0; nt < NT; ++nt)
+                    nb2[nt] = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
 #pragma unroll
                 for (int k = 0; k < KSTEP_PER_G; ++k) {
                     const int ks = g * KSTEP_PER_G + k;
@@ -383,8 +391,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                             ldsm_x2(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
                             b10 = b11 = 0u;
                         }
-                        mma16816(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01);
-                        if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11);
+                        if (k == 0) {
+                            const float2 c = nb2[2 * np];
+                            mma16816_c(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01, c.x, c.y, c.x, c.y);
+                            if (2 * np + 1 < NT) {
+                                const float2 c1 = nb2[2 * np + 1];
+                                mma16816_c(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11, c1.x, c1.y, c1.x, c1.y);
+                            }
+                        } else {
+                            mma16816(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01);
+                            if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11);
+                        }
                     }
                 }
 #pragma unroll
@@ -487,11 +504,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
                 float sv[4];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int tk = 16 * kk + 2 * tig + (qq & 1) + 8 * (qq >> 1);
-                    sv[qq] = (t_tile + tk < hi) ? __half2float(reinterpret_cast<const __half *>(vsp + tk * C::VSB)[g_w])
-                                                : 0.0f;
+                {
+                    const float2 s01 =
+                        __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig));
+                    const float2 s89 =
+                        __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig + 8));
+                    sv[0] = s01.x;
+                    sv[1] = s01.y;
+                    sv[2] = s89.x;
+                    sv[3] = s89.y;
                 }
                 uint32_t b0[NT], b1[NT];
 #pragma unroll
