@@ -169,14 +169,18 @@ __device__ __forceinline__ void issue_tile(uint32_t base, uint32_t full, const C
                                            const CUtensorMap *tmv, const uint8_t *ksc, const uint8_t *vsc,
                                            int64_t row0)
 {
+    // the cache is read once per call: evict-first in L2
+    const uint64_t pol = evict_first_policy();
     mbar_expect_tx(full, (uint32_t)(KG::BYTES + VG::BYTES + kTile * (C::KSB + C::VSB)));
     const int y = (int)row0;
 #pragma unroll
-    for (int b = 0; b < KG::NB; ++b) tma_load_2d(base + C::K_OFF + b * kTile * KG::BI, tmk, b * KG::BI, y, full);
+    for (int b = 0; b < KG::NB; ++b)
+        tma_load_2d(base + C::K_OFF + b * kTile * KG::BI, tmk, b * KG::BI, y, full, pol);
 #pragma unroll
-    for (int b = 0; b < VG::NB; ++b) tma_load_2d(base + C::V_OFF + b * kTile * VG::BI, tmv, b * VG::BI, y, full);
-    bulk_load(base + C::KS_OFF, ksc + row0 * C::KSB, kTile * C::KSB, full);
-    bulk_load(base + C::VS_OFF, vsc + row0 * C::VSB, kTile * C::VSB, full);
+    for (int b = 0; b < VG::NB; ++b)
+        tma_load_2d(base + C::V_OFF + b * kTile * VG::BI, tmv, b * VG::BI, y, full, pol);
+    bulk_load_hint(base + C::KS_OFF, ksc + row0 * C::KSB, kTile * C::KSB, full, pol);
+    bulk_load_hint(base + C::VS_OFF, vsc + row0 * C::VSB, kTile * C::VSB, full, pol);
 }
 
 template <int KC, int D, int NT, typename QT>
