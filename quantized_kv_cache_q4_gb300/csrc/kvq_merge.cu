@@ -111,12 +111,22 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
                          float *out, float *out_lse, cudaStream_t st)
 {
     if (rows == 0) return cudaSuccess;
-    // lanes per column: enough that a lane loads at most kUnroll splits, fewer
-    // while that would take more than about two waves of threads
+    // lanes per column: enough that a lane loads at most kUnroll splits per
+    // round, fewer while that would take more than about half a wave of threads
+    // (measured: with many rows, fewer lanes each streaming more splits win)
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    int n_sm = (dev >= 0 && dev < 64) ? sms[dev] : 0;
+    if (n_sm <= 0) {
+        if (dev < 0 || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+            n_sm = 152;
+        if (dev >= 0 && dev < 64) sms[dev] = n_sm;
+    }
     int lpc = 1;
     while (lpc < 32 && lpc * kUnroll < n_splits) lpc *= 2;
     const int64_t items = (int64_t)rows * (head_dim / 4);
-    while (lpc > 1 && items * lpc > 2LL * 152 * 2048) lpc /= 2;
+    while (lpc > 1 && items * lpc > (int64_t)n_sm * 1024) lpc /= 2;
     switch (lpc) {
     case 1: return launch_lpc<1>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
     case 2: return launch_lpc<2>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
