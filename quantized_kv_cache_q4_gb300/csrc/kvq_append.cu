@@ -111,15 +111,16 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
     const int i = (int)(si % a.n_new);
     const int s = (int)(si / a.n_new);
 
+    // the source row does not depend on the position: both loads in flight at once
+    constexpr int D = VPL * 32;
+    const SrcT *src = static_cast<const SrcT *>(pl ? a.src[1] : a.src[0]) + src_row * D + lane * VPL;
+    float x[VPL];
+    load_vals<VPL>(src, x);
     const int p0 = a.pos0[s];
     if (p0 < 0 || (int64_t)p0 + a.n_new > a.capacity) {
         if (lane == 0 && i == 0 && h == 0 && pl == 0 && a.err) atomicOr(a.err, KVQ_ERR_APPEND_POS);
         return;
     }
-    constexpr int D = VPL * 32;
-    const SrcT *src = static_cast<const SrcT *>(pl ? a.src[1] : a.src[0]) + src_row * D + lane * VPL;
-    float x[VPL];
-    load_vals<VPL>(src, x);
     float amax = 0.0f;
 #pragma unroll
     for (int v = 0; v < VPL; ++v) amax = fmaxf(amax, fabsf(x[v]));
