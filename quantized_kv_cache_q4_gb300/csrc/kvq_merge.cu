@@ -111,9 +111,10 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
                          float *out, float *out_lse, cudaStream_t st)
 {
     if (rows == 0) return cudaSuccess;
-    // lanes per column: enough that a lane loads at most kUnroll splits per
-    // round, fewer while that would take more than about half a wave of threads
-    // (measured: with many rows, fewer lanes each streaming more splits win)
+    // lanes per column: enough that a lane loads at most two rounds of kUnroll
+    // splits, fewer while that would take more than about a quarter wave of
+    // threads (measured on GB300: 114 splits x 24 rows is fastest with 16 lanes,
+    // 29 splits x 1152 rows with one lane per column)
     static int sms[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
@@ -124,9 +125,9 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
         if (dev >= 0 && dev < 64) sms[dev] = n_sm;
     }
     int lpc = 1;
-    while (lpc < 32 && lpc * kUnroll < n_splits) lpc *= 2;
+    while (lpc < 32 && lpc * 2 * kUnroll < n_splits) lpc *= 2;
     const int64_t items = (int64_t)rows * (head_dim / 4);
-    while (lpc > 1 && items * lpc > (int64_t)n_sm * 1024) lpc /= 2;
+    while (lpc > 1 && items * lpc > (int64_t)n_sm * 512) lpc /= 2;
     switch (lpc) {
     case 1: return launch_lpc<1>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
     case 2: return launch_lpc<2>(po, pl, n_splits, rows, head_dim, out, out_lse, st);
