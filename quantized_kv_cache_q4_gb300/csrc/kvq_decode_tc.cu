@@ -320,120 +320,114 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mg[nt] = -INFINITY, lg[nt] = 0.0f;
 
-    for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kS;
-        if (!s_timeout && !mbar_wait(bar_full + 8 * st, (j / kS) & 1)) s_timeout = 1;
-        // the barrier below needs all four warps every tile: after a timeout the
-        // warps keep stepping with masked data instead of leaving
-        const bool dead = __any_sync(0xffffffffu, s_timeout != 0);
-        const int t_tile = lo + j * kTile;
-        const int tb = t_tile + tl;
+    // ---- phase A of tile jj: S^T for this warp's 16 tokens (log2 units, not yet
+    // masked) and the tile's V scales transposed for phase B (0 past the split end)
+    auto phase_a = [&](int jj, float (&sc)[NT][4]) {
+        const int st = jj % kS;
+        const int tb = lo + jj * kTile + tl;
         const uint32_t base = smem_u32(smem + st * C::STAGE);
         const uint8_t *ksp = smem + st * C::STAGE + C::KS_OFF;
         const uint8_t *vsp = smem + st * C::STAGE + C::VS_OFF;
-        float *s_s = s_s0 + (j & 1) * (kTile * C::PS);
-        float *red_m = red_m0 + (j & 1) * (kW * 32);
-        __half *vt = vt0 + (j & 1) * (C::NGV * kTile);
-        // this warp's 16 tokens' V scales, transposed for phase B (0 past the split end)
+        __half *vt = vt0 + (jj & 1) * (C::NGV * kTile);
         for (int i = lane; i < 16 * C::NGV; i += 32) {
             const int t = i & 15, g = i >> 4;
             vt[g * kTile + tl + t] =
                 (tb + t < hi) ? reinterpret_cast<const __half *>(vsp + (tl + t) * C::VSB)[g] : __float2half_rn(0.0f);
         }
-
-        // ---- phase A: S^T for this warp's 16 tokens ----
-        float sc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) sc[nt][c] = 0.0f;
-        if (tb < hi && !dead) {
-            float sk0[NGK], sk1[NGK];
-            load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
-            load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
+        float sk0[NGK], sk1[NGK];
+        load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
+        load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
 #pragma unroll
-            for (int g = 0; g < NGK; ++g) {
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4(base + koff[g], r0, r1, r2, r3);
-                uint32_t h0[4], h1[4], h2[4], h3[4];
-                if constexpr (KC == KVQ_CODEC_Q4_G64) {
-                    unpack_q4_biased(r0, h0);
-                    unpack_q4_biased(r1, h1);
-                    unpack_q4_biased(r2, h2);
-                    unpack_q4_biased(r3, h3);
-                } else {
-                    uint32_t t2[2];
-                    unpack_q8_biased(r0, t2); h0[0] = t2[0]; h0[1] = t2[1];
-                    unpack_q8_biased(r1, t2); h1[0] = t2[0]; h1[1] = t2[1];
-                    unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
-                    unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
-                }
-                // each group's accumulator starts at minus its bias term (the first
-                // k-step's MMA takes it as its accumulator input)
-                float cg[NT][4];
-                float2 nb2[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    nb2[nt] = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
-#pragma unroll
-                for (int k = 0; k < KSTEP_PER_G; ++k) {
-                    const int ks = g * KSTEP_PER_G + k;
-#pragma unroll
-                    for (int np = 0; np < (NT + 1) / 2; ++np) {
-                        // B fragments of n-tiles 2np and 2np+1 (the second exists only
-                        // when 2np + 1 < NT)
-                        uint32_t b00, b01, b10, b11;
-                        if constexpr (QREG) {
-                            b00 = qf[ks][0];
-                            b01 = qf[ks][1];
-                            b10 = b11 = 0u;
-                        } else if (2 * np + 1 < NT) {
-                            const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
-                            ldsm_x4(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
-                        } else {
-                            const int qrow = 2 * np * 8 + (lane & 7);
-                            ldsm_x2(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
-                            b10 = b11 = 0u;
-                        }
-                        if (k == 0) {
-                            const float2 c = nb2[2 * np];
-                            mma16816_c(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01, c.x, c.y, c.x, c.y);
-                            if (2 * np + 1 < NT) {
-                                const float2 c1 = nb2[2 * np + 1];
-                                mma16816_c(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11, c1.x, c1.y, c1.x, c1.y);
-                            }
-                        } else {
-                            mma16816(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01);
-                            if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    sc[nt][0] = fmaf(cg[nt][0], sk0[g], sc[nt][0]);
-                    sc[nt][1] = fmaf(cg[nt][1], sk0[g], sc[nt][1]);
-                    sc[nt][2] = fmaf(cg[nt][2], sk1[g], sc[nt][2]);
-                    sc[nt][3] = fmaf(cg[nt][3], sk1[g], sc[nt][3]);
-                }
+        for (int g = 0; g < NGK; ++g) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(base + koff[g], r0, r1, r2, r3);
+            uint32_t h0[4], h1[4], h2[4], h3[4];
+            if constexpr (KC == KVQ_CODEC_Q4_G64) {
+                unpack_q4_biased(r0, h0);
+                unpack_q4_biased(r1, h1);
+                unpack_q4_biased(r2, h2);
+                unpack_q4_biased(r3, h3);
+            } else {
+                uint32_t t2[2];
+                unpack_q8_biased(r0, t2); h0[0] = t2[0]; h0[1] = t2[1];
+                unpack_q8_biased(r1, t2); h1[0] = t2[0]; h1[1] = t2[1];
+                unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
+                unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
             }
+            // each group's accumulator starts at minus its bias term (the first
+            // k-step's MMA takes it as its accumulator input)
+            float cg[NT][4];
+            float2 nb2[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
+                nb2[nt] = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) sc[nt][c] *= sl2;
-        }
-        {
-            const int ta = tb + gid, tc = ta + 8;
-            if (dead || tb + 16 > hi || tb + 16 > nv_min) {
+            for (int k = 0; k < KSTEP_PER_G; ++k) {
+                const int ks = g * KSTEP_PER_G + k;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (dead || !(ta < hi && ta < nv[nt][0])) sc[nt][0] = -INFINITY;
-                    if (dead || !(ta < hi && ta < nv[nt][1])) sc[nt][1] = -INFINITY;
-                    if (dead || !(tc < hi && tc < nv[nt][0])) sc[nt][2] = -INFINITY;
-                    if (dead || !(tc < hi && tc < nv[nt][1])) sc[nt][3] = -INFINITY;
+                for (int np = 0; np < (NT + 1) / 2; ++np) {
+                    // B fragments of n-tiles 2np and 2np+1 (the second exists only
+                    // when 2np + 1 < NT)
+                    uint32_t b00, b01, b10, b11;
+                    if constexpr (QREG) {
+                        b00 = qf[ks][0];
+                        b01 = qf[ks][1];
+                        b10 = b11 = 0u;
+                    } else if (2 * np + 1 < NT) {
+                        const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
+                        ldsm_x4(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
+                    } else {
+                        const int qrow = 2 * np * 8 + (lane & 7);
+                        ldsm_x2(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
+                        b10 = b11 = 0u;
+                    }
+                    if (k == 0) {
+                        const float2 c = nb2[2 * np];
+                        mma16816_c(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01, c.x, c.y, c.x, c.y);
+                        if (2 * np + 1 < NT) {
+                            const float2 c1 = nb2[2 * np + 1];
+                            mma16816_c(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11, c1.x, c1.y, c1.x, c1.y);
+                        }
+                    } else {
+                        mma16816(cg[2 * np], h0[k], h1[k], h2[k], h3[k], b00, b01);
+                        if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], h0[k], h1[k], h2[k], h3[k], b10, b11);
+                    }
                 }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                sc[nt][0] = fmaf(cg[nt][0], sk0[g], sc[nt][0]);
+                sc[nt][1] = fmaf(cg[nt][1], sk0[g], sc[nt][1]);
+                sc[nt][2] = fmaf(cg[nt][2], sk1[g], sc[nt][2]);
+                sc[nt][3] = fmaf(cg[nt][3], sk1[g], sc[nt][3]);
+            }
         }
-        // scores and this warp's per-row maximum of the tile, for phase B
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[nt][c] *= sl2;
+    };
+
+    // ---- end of phase A: mask (split end, causal rows), store the scores and
+    // this warp's per-row maximum of the tile for phase B
+    auto phase_a_store = [&](int jj, float (&sc)[NT][4]) {
+        const int tb = lo + jj * kTile + tl;
+        const int ta = tb + gid, tc = ta + 8;
+        if (tb + 16 > hi || tb + 16 > nv_min) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (!(ta < hi && ta < nv[nt][0])) sc[nt][0] = -INFINITY;
+                if (!(ta < hi && ta < nv[nt][1])) sc[nt][1] = -INFINITY;
+                if (!(tc < hi && tc < nv[nt][0])) sc[nt][2] = -INFINITY;
+                if (!(tc < hi && tc < nv[nt][1])) sc[nt][3] = -INFINITY;
+            }
+        }
+        float *s_s = s_s0 + (jj & 1) * (kTile * C::PS);
+        float *red_m = red_m0 + (jj & 1) * (kW * 32);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             *reinterpret_cast<float2 *>(s_s + (tl + gid) * C::PS + nt * 8 + 2 * tig) = make_float2(sc[nt][0], sc[nt][1]);
@@ -447,22 +441,18 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             }
             if (gid == 0) *reinterpret_cast<float2 *>(red_m + warp * 32 + nt * 8 + 2 * tig) = make_float2(mx0, mx1);
         }
-        // The one barrier of the tile.  It also orders every warp's reads of
-        // tile j - 1 (previous phase B) before the refill of that tile's stage.
-        warps_sync();
-        if (threadIdx.x == 0 && j >= 1 && !s_timeout) {
-            const int jn = j - 1 + kS;
-            if (jn < n_tiles) {
-                issue_tile<C, KG, VG>(smem_u32(smem + ((j - 1) % kS) * C::STAGE), bar_full + 8 * ((j - 1) % kS), &tmk,
-                                      &tmv, ksc, vsc, plane_row + lo + jn * kTile);
-                s_issued = jn + 1;
-            }
-        }
+    };
 
-        // ---- phase B: softmax of the tile and O^T += V^T P'^T for this warp's head_dim slice ----
+    // ---- phase B of tile jj: softmax of the tile and O^T += V^T P'^T for this
+    // warp's head_dim slice
+    auto phase_b = [&](int jj) {
+        const int st = jj % kS;
+        const uint32_t base = smem_u32(smem + st * C::STAGE);
+        const float *s_s = s_s0 + (jj & 1) * (kTile * C::PS);
+        const float *red_m = red_m0 + (jj & 1) * (kW * 32);
+        const __half *vt = vt0 + (jj & 1) * (C::NGV * kTile);
         // new running maximum of row nt * 8 + gid (the same in every warp)
         float cf[NT];
-        bool grow = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int r = nt * 8 + gid;
@@ -471,84 +461,120 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             for (int w = 1; w < kW; ++w) tmax = fmaxf(tmax, red_m[w * 32 + r]);
             const float mn = fmaxf(mg[nt], tmax);
             cf[nt] = (mn == -INFINITY) ? 1.0f : ex2(mg[nt] - mn);
-            grow |= mn > mg[nt];
             mg[nt] = mn;
             lg[nt] *= cf[nt];
         }
-        if (__any_sync(0xffffffffu, grow)) {
-            // accumulator columns are rows 2 tig and 2 tig + 1: their factors come from
-            // the lanes whose fragment row they are
+        // accumulator columns are rows 2 tig and 2 tig + 1: their factors come from
+        // the lanes whose fragment row they are (1 unless the maximum grew)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float c0 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig);
-                const float c1 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig + 4);
+        for (int nt = 0; nt < NT; ++nt) {
+            const float c0 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig);
+            const float c1 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig + 4);
 #pragma unroll
-                for (int t = 0; t < MTW; ++t) {
-                    o[t][nt][0] *= c0;
-                    o[t][nt][1] *= c1;
-                    o[t][nt][2] *= c0;
-                    o[t][nt][3] *= c1;
-                }
+            for (int t = 0; t < MTW; ++t) {
+                o[t][nt][0] *= c0;
+                o[t][nt][1] *= c1;
+                o[t][nt][2] *= c0;
+                o[t][nt][3] *= c1;
             }
         }
-        if (!dead) {
-            float msub[NT];
+        float msub[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
-            // sum over the tile's tokens of P' per row (the same in all 16 accumulator
-            // rows), for removing the codes' fp16 bias once per tile
-            float psum[NT][4];
+        for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
+        // sum over the tile's tokens of P' per row (the same in all 16 accumulator
+        // rows), for removing the codes' fp16 bias once per tile
+        float psum[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) psum[nt][c] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+            // tokens past the split end have score -inf (p = 0) and V scale 0
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig));
+            const float2 s89 =
+                __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig + 8));
+            uint32_t b0[NT], b1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float *sr = s_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
+                const float p0 = ex2(sr[0] - msub[nt]), p1 = ex2(sr[C::PS] - msub[nt]);
+                const float p2 = ex2(sr[8 * C::PS] - msub[nt]), p3 = ex2(sr[9 * C::PS] - msub[nt]);
+                lg[nt] += (p0 + p1) + (p2 + p3);
+                b0[nt] = pack_f16x2(p0 * s01.x, p1 * s01.y);
+                b1[nt] = pack_f16x2(p2 * s89.x, p3 * s89.y);
+            }
+            constexpr uint32_t kOnes = 0x3C003C00u;                 // fp16x2 (1, 1)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(psum[nt], kOnes, kOnes, kOnes, kOnes, b0[nt], b1[nt]);
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+                const int e = e0 + t;
+                const uint32_t a0 = q4_pair_biased(r0, e), a1 = q4_pair_biased(r1, e);
+                const uint32_t a2 = q4_pair_biased(r2, e), a3 = q4_pair_biased(r3, e);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
+            }
+        }
+        // remove the bias: 1032 per P' for even nibble pairs, 1152 for odd ones
+#pragma unroll
+        for (int t = 0; t < MTW; ++t) {
+            const float cb = ((e0 + t) & 1) ? -1152.0f : -1032.0f;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) psum[nt][c] = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                // tokens past the split end have score -inf (p = 0) and V scale 0
-                uint32_t r0, r1, r2, r3;
-                ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
-                float sv[4];
-                {
-                    const float2 s01 =
-                        __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig));
-                    const float2 s89 =
-                        __half22float2(*reinterpret_cast<const __half2 *>(vt + g_w * kTile + 16 * kk + 2 * tig + 8));
-                    sv[0] = s01.x;
-                    sv[1] = s01.y;
-                    sv[2] = s89.x;
-                    sv[3] = s89.y;
-                }
-                uint32_t b0[NT], b1[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float *sr = s_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
-                    const float p0 = ex2(sr[0] - msub[nt]), p1 = ex2(sr[C::PS] - msub[nt]);
-                    const float p2 = ex2(sr[8 * C::PS] - msub[nt]), p3 = ex2(sr[9 * C::PS] - msub[nt]);
-                    lg[nt] += (p0 + p1) + (p2 + p3);
-                    b0[nt] = pack_f16x2(p0 * sv[0], p1 * sv[1]);
-                    b1[nt] = pack_f16x2(p2 * sv[2], p3 * sv[3]);
-                }
-                constexpr uint32_t kOnes = 0x3C003C00u;                 // fp16x2 (1, 1)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(psum[nt], kOnes, kOnes, kOnes, kOnes, b0[nt], b1[nt]);
-#pragma unroll
-                for (int t = 0; t < MTW; ++t) {
-                    const int e = e0 + t;
-                    const uint32_t a0 = q4_pair_biased(r0, e), a1 = q4_pair_biased(r1, e);
-                    const uint32_t a2 = q4_pair_biased(r2, e), a3 = q4_pair_biased(r3, e);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[nt], b1[nt]);
-                }
+                for (int c = 0; c < 4; ++c) o[t][nt][c] = fmaf(cb, psum[nt][c], o[t][nt][c]);
+        }
+    };
+
+    if constexpr (NT == 1) {
+        // Software-pipelined tile loop: iteration j runs phase A of tile j + 1 and
+        // phase B of tile j, two independent instruction streams in one block (the
+        // scores, maxima and transposed V scales are double-buffered by tile
+        // parity), then the one CTA barrier, which also orders every warp's reads
+        // of tile j before its stage is refilled with tile j + kS.  The last
+        // tile's phase B runs alone.  After a timeout the waits are skipped and
+        // the warps keep stepping over stale data (the result is flagged as
+        // invalid), so every warp reaches every barrier.
+        if (n_tiles > 0) {
+            if (!s_timeout && !mbar_wait(bar_full, 0)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(0, sc);
+            phase_a_store(0, sc);
+        }
+        warps_sync();
+        for (int j = 0; j + 1 < n_tiles; ++j) {
+            if (!s_timeout && !mbar_wait(bar_full + 8 * ((j + 1) % kS), ((j + 1) / kS) & 1)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(j + 1, sc);
+            phase_b(j);
+            phase_a_store(j + 1, sc);
+            warps_sync();
+            if (threadIdx.x == 0 && !s_timeout && j + kS < n_tiles) {
+                issue_tile<C, KG, VG>(smem_u32(smem + (j % kS) * C::STAGE), bar_full + 8 * (j % kS), &tmk, &tmv, ksc,
+                                      vsc, plane_row + lo + (j + kS) * kTile);
+                s_issued = j + kS + 1;
             }
-            // remove the bias: 1032 per P' for even nibble pairs, 1152 for odd ones
-#pragma unroll
-            for (int t = 0; t < MTW; ++t) {
-                const float cb = ((e0 + t) & 1) ? -1152.0f : -1032.0f;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) o[t][nt][c] = fmaf(cb, psum[nt][c], o[t][nt][c]);
+        }
+        if (n_tiles > 0) phase_b(n_tiles - 1);
+    } else {
+        // Several n-tiles: registers do not allow both phases at once.  Per tile:
+        // phase A, the one CTA barrier (which also orders every warp's reads of
+        // tile j - 1 before that stage is refilled with tile j - 1 + kS), phase B.
+        for (int j = 0; j < n_tiles; ++j) {
+            if (!s_timeout && !mbar_wait(bar_full + 8 * (j % kS), (j / kS) & 1)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(j, sc);
+            phase_a_store(j, sc);
+            warps_sync();
+            if (threadIdx.x == 0 && j >= 1 && !s_timeout && j - 1 + kS < n_tiles) {
+                issue_tile<C, KG, VG>(smem_u32(smem + ((j - 1) % kS) * C::STAGE), bar_full + 8 * ((j - 1) % kS), &tmk,
+                                      &tmv, ksc, vsc, plane_row + lo + (j - 1 + kS) * kTile);
+                s_issued = j - 1 + kS + 1;
             }
+            phase_b(j);
         }
     }
     // the dependent launch (the merge of the splits) may start now: its CTAs
