@@ -25,7 +25,9 @@ import numpy as np
 
 Q4_G64 = 1
 Q8_0 = 2
-GROUP = {Q4_G64: 64, Q8_0: 32}
+Q4_G32 = 3                  # the pages' "q4_0", read as Q4_G64 with 32-value groups
+GROUP = {Q4_G64: 64, Q8_0: 32, Q4_G32: 32}
+FOUR_BIT = (Q4_G64, Q4_G32)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
@@ -107,7 +109,7 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def row_bytes(codec: int, head_dim: int) -> int:
-    return head_dim // 2 if codec == Q4_G64 else head_dim
+    return head_dim // 2 if codec in FOUR_BIT else head_dim
 
 
 def scales_per_row(codec: int, head_dim: int) -> int:

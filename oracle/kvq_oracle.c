@@ -15,6 +15,11 @@
  *     reference and the dequantizer bit-identical).  The pages give no rounding
  *     rule; the rule used is scale = fp16(absmax / 7), q = clamp(rne(x / scale),
  *     -8, 7), with the division by the fp16-rounded scale widened to fp32.
+ *   - Q4_G32: the "q4_0" V cache of the shipped pair "-ctk q8_0 -ctv q4_0"
+ *     (den_llama.cpp, "What's in the fork": the q8_0-q4_0 FlashAttention pair;
+ *     "Results": the 65K serve run) is not defined on the pages; it is read as
+ *     the Q4_G64 rule and nibble layout with groups of 32 values (4.5 bits per
+ *     value).
  *   - The q8_0-style K codec of the mixed pair "-ctk q8_0 -ctv q4_g64"
  *     (den_llama.cpp, "Build3 (working engine)" command block): 32 int8 values
  *     with one FP16 scale, scale = fp16(absmax / 127), q = clamp(rne(x/scale),
@@ -42,6 +47,7 @@
 
 #define ORC_Q4 1
 #define ORC_Q8 2
+#define ORC_Q4_32 3
 
 /* ------------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> binary32, written from the format definition.      */
@@ -108,14 +114,16 @@ void orc_f16_to_f32_array(const uint16_t *h, int64_t n, float *out)
 /* Codec                                                                    */
 /* ------------------------------------------------------------------------ */
 
+/* 4-bit codecs: Q4_G64 and Q4_G32 (the same rule and nibble layout with 32-value groups). */
+static int orc_is4(int codec) { return codec == ORC_Q4 || codec == ORC_Q4_32; }
 static int orc_group(int codec) { return codec == ORC_Q4 ? 64 : 32; }
-static int orc_qmax(int codec) { return codec == ORC_Q4 ? 7 : 127; }
-static int orc_qmin(int codec) { return codec == ORC_Q4 ? -8 : -127; }
+static int orc_qmax(int codec) { return orc_is4(codec) ? 7 : 127; }
+static int orc_qmin(int codec) { return orc_is4(codec) ? -8 : -127; }
 
 /* Bytes of the code plane per row of head_dim values. */
 int orc_row_bytes(int codec, int head_dim)
 {
-    return codec == ORC_Q4 ? head_dim / 2 : head_dim;
+    return orc_is4(codec) ? head_dim / 2 : head_dim;
 }
 
 int orc_scales_per_row(int codec, int head_dim) { return head_dim / orc_group(codec); }
@@ -150,6 +158,7 @@ static int orc_code(float x, float d, int qmin, int qmax)
  * Q4_G64: qs row = head_dim/2 bytes; byte j holds value 2j in its low nibble
  *         and value 2j+1 in its high nibble, each as a 4-bit two's complement
  *         code; scales row = head_dim/64 fp16 bit patterns, group order.
+ * Q4_G32: the same with groups of 32 values (head_dim/32 scales).
  * Q8_0:   qs row = head_dim int8 codes; scales row = head_dim/32 fp16. */
 void orc_quantize(int codec, const float *x, int64_t n_rows, int head_dim,
                   uint8_t *qs, uint16_t *scales)
@@ -167,7 +176,7 @@ void orc_quantize(int codec, const float *x, int64_t n_rows, int head_dim,
             for (int i = 0; i < gs; ++i) {
                 int q = orc_code(xg[i], d, qmin, qmax);
                 int v = g * gs + i;
-                if (codec == ORC_Q4) {
+                if (orc_is4(codec)) {
                     uint8_t nib = (uint8_t)(q & 0xF);
                     if (v & 1) qr[v >> 1] = (uint8_t)((qr[v >> 1] & 0x0F) | (nib << 4));
                     else       qr[v >> 1] = (uint8_t)((qr[v >> 1] & 0xF0) | nib);
@@ -182,7 +191,7 @@ void orc_quantize(int codec, const float *x, int64_t n_rows, int head_dim,
 /* Code of value v of a row, as a signed integer. */
 static int orc_get_code(int codec, const uint8_t *qr, int v)
 {
-    if (codec == ORC_Q4) {
+    if (orc_is4(codec)) {
         int nib = (v & 1) ? (qr[v >> 1] >> 4) : (qr[v >> 1] & 0xF);
         return nib >= 8 ? nib - 16 : nib;
     }

@@ -1,9 +1,10 @@
-"""Pins the oracle's Q4_G64 and q8_0 codec.
+"""Pins the oracle's Q4_G64, Q4_G32 and q8_0 codecs.
 
 What fixes the codec: signed INT4 with one FP16 scale per 64 values, exactly
 4.25 bits/value (den_llama.cpp, "What this fork is", quantized KV cache
 bullet); the q8_0-style K of the mixed pair (den_llama.cpp, "Build3 (working
-engine)" command block).  Rounding rule: scale = fp16(absmax/qmax), code =
+engine)" command block); the pages' "q4_0" V, read as the Q4_G64 rule with
+32-value groups (Q4_G32, exactly 4.5 bits/value).  Rounding rule: scale = fp16(absmax/qmax), code =
 clamp(rne(x/scale)).  Pins: the storage closed form, hand-worked golden rows,
 exact rational brute force of the nearest code, the round-trip bound, special
 blocks, exact dequantization, and the append semantics."""
@@ -16,8 +17,9 @@ import pytest
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-QRANGE = {oracle.Q4_G64: (-8, 7), oracle.Q8_0: (-127, 127)}
-QMAX = {oracle.Q4_G64: 7, oracle.Q8_0: 127}
+QRANGE = {oracle.Q4_G64: (-8, 7), oracle.Q8_0: (-127, 127), oracle.Q4_G32: (-8, 7)}
+QMAX = {oracle.Q4_G64: 7, oracle.Q8_0: 127, oracle.Q4_G32: 7}
+CODECS = (oracle.Q4_G64, oracle.Q8_0, oracle.Q4_G32)
 
 
 def _load_golden(name):
@@ -43,7 +45,8 @@ def _codes(codec, qs, head_dim):
 
 
 @pytest.mark.parametrize("name,codec", [("q4g64_two_groups.txt", oracle.Q4_G64),
-                                        ("q8_0_two_groups.txt", oracle.Q8_0)])
+                                        ("q8_0_two_groups.txt", oracle.Q8_0),
+                                        ("q4g32_two_groups.txt", oracle.Q4_G32)])
 def test_golden_rows(name, codec):
     g = _load_golden(name)
     x = np.array([float(v) for v in g["x"]], np.float32)
@@ -57,7 +60,8 @@ def test_golden_rows(name, codec):
     assert np.array_equal(xh.astype(np.float64), d * _codes(codec, qs, x.size)[0])
 
 
-@pytest.mark.parametrize("codec,bpv", [(oracle.Q4_G64, Fraction(17, 4)), (oracle.Q8_0, Fraction(17, 2))])
+@pytest.mark.parametrize("codec,bpv", [(oracle.Q4_G64, Fraction(17, 4)), (oracle.Q8_0, Fraction(17, 2)),
+                                       (oracle.Q4_G32, Fraction(9, 2))])
 @pytest.mark.parametrize("head_dim", [64, 128, 256, 512])
 def test_storage_closed_form(codec, bpv, head_dim):
     rows = 37
@@ -75,7 +79,7 @@ def _groups(rng, n, gs):
     return x.astype(np.float32)
 
 
-@pytest.mark.parametrize("codec", [oracle.Q4_G64, oracle.Q8_0])
+@pytest.mark.parametrize("codec", CODECS)
 def test_brute_force_nearest_code(codec):
     """Each code is the nearest integer in range to x/scale (exact rational
     distance), ties to even, except within 2^-20 of a tie where the fp32
@@ -104,7 +108,7 @@ def test_brute_force_nearest_code(codec):
     assert (codes == nearest_even).mean() > 0.999
 
 
-@pytest.mark.parametrize("codec", [oracle.Q4_G64, oracle.Q8_0])
+@pytest.mark.parametrize("codec", CODECS)
 def test_scale_rule_and_roundtrip_bound(codec):
     gs = oracle.GROUP[codec]
     rng = np.random.Generator(np.random.PCG64(12))
@@ -130,7 +134,7 @@ def test_scale_rule_and_roundtrip_bound(codec):
     assert np.all(np.abs(c[sel]) == QMAX[codec])
 
 
-@pytest.mark.parametrize("codec", [oracle.Q4_G64, oracle.Q8_0])
+@pytest.mark.parametrize("codec", CODECS)
 def test_special_blocks(codec):
     gs, qm = oracle.GROUP[codec], QMAX[codec]
     zero = np.zeros((1, 2 * gs), np.float32)
@@ -164,7 +168,7 @@ def test_minus_eight_decodes():
 
 def test_dequant_exact_in_fp64():
     rng = np.random.Generator(np.random.PCG64(13))
-    for codec in (oracle.Q4_G64, oracle.Q8_0):
+    for codec in CODECS:
         x = rng.standard_normal((200, 256)).astype(np.float32) * 3
         qs, sc = oracle.quantize(codec, x)
         xh = oracle.dequantize(codec, qs, sc, 256)
@@ -183,7 +187,7 @@ def test_fp16_sources_quantize_like_their_fp32_widening():
 def test_append_positions_and_error_bit():
     rng = np.random.Generator(np.random.PCG64(15))
     S, n_new, Hk, D, cap = 3, 2, 2, 128, 8
-    for codec in (oracle.Q4_G64, oracle.Q8_0):
+    for codec in CODECS:
         cache = oracle.Cache(codec, S, Hk, D, cap)
         src = rng.standard_normal((S, n_new, Hk, D)).astype(np.float32)
         pos0 = np.array([0, 6, 7], np.int32)          # the last one overflows capacity

@@ -9,11 +9,12 @@ import test_oracle_attention as ta
 import test_oracle_codec as tc
 import test_oracle_fp16 as tf
 
-Q4, Q8 = oracle.Q4_G64, oracle.Q8_0
+Q4, Q8, Q4_32 = oracle.Q4_G64, oracle.Q8_0, oracle.Q4_G32
 
 PINS = [
     ("golden q4", lambda: tc.test_golden_rows("q4g64_two_groups.txt", Q4)),
     ("golden q8", lambda: tc.test_golden_rows("q8_0_two_groups.txt", Q8)),
+    ("golden q4 g32", lambda: tc.test_golden_rows("q4g32_two_groups.txt", Q4_32)),
     ("fp16 edges", tf.test_f32_to_f16_edge_classes),
     ("fp16 dense", tf.test_f32_to_f16_half_range_dense),
     ("brute force q4", lambda: tc.test_brute_force_nearest_code(Q4)),
@@ -34,6 +35,8 @@ MUTANTS = {
     "round_half_away": ("float r = nearbyintf(x / d);", "float r = roundf(x / d);"),
     "no_saturation": ("if (d == 0x7C00u) d = 0x7BFFu;", ""),
     "q8_group": ("return codec == ORC_Q4 ? 64 : 32;", "return codec == ORC_Q4 ? 64 : 64;"),
+    "q4_g32_group": ("static int orc_group(int codec) { return codec == ORC_Q4 ? 64 : 32; }",
+                     "static int orc_group(int codec) { return (codec == ORC_Q4 || codec == ORC_Q4_32) ? 64 : 32; }"),
     "f16_truncates": ("if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;", ""),
     "f16_subnormal_shift": ("uint32_t shift = 126u - e;", "uint32_t shift = 127u - e;"),
     "gqa_mapping": ("int r = i * G + j, h = kh * G + j;", "int r = i * G + j, h = kh + j * a->n_kv_heads;"),

@@ -4,7 +4,7 @@ This module only draws random numbers and lays them out; it holds none of the
 codec or attention arithmetic, so that both the CUDA path and the oracle can be
 fed the same arrays without sharing any of the method's code.
 
-The five workloads stand in for the long-context decode and MTP-verify runs of
+Workloads 0-4 stand in for the long-context decode and MTP-verify runs of
 a 27B hybrid model described on den_llama.cpp ("Results": 32K and 65K serving
 with MTP n-max 2; "What this fork is": up to 196K context; "Build3 (working
 engine)": the matched Q4_G64 pair and the mixed q8_0-K / Q4_G64-V pair).  No
@@ -28,6 +28,9 @@ V bias, the outlier mask and the sequence lengths):
   4 mtp16     S=16, L_s = round(exp(U(ln 1024, ln 65536))) cached tokens,
               3 appended tokens per sequence (1 + 2 draft), n_q=3 (causal),
               K/V/Q fp16 ~ N(0,1); Q4_G64 K and V.
+  5 ship65k   as 2 with K q8_0 / V Q4_G32 (the pages' shipped -ctk q8_0 -ctv q4_0
+              pair, q4_0 read as Q4 with 32-value groups); not a benchmark
+              workload, it carries that pair through the same tests.
 """
 from __future__ import annotations
 
@@ -39,6 +42,7 @@ import numpy as np
 
 Q4_G64 = 1
 Q8_0 = 2
+Q4_G32 = 3
 BASE_SEED = 20261202
 TOKEN_ALIGN = 64          # cache capacity is a multiple of this many tokens
 
@@ -82,10 +86,12 @@ def spec(index: int) -> Spec:
     if index == 4:
         return Spec("mtp16", 16, 24, 4, 256, None, 3, Q4_G64, Q4_G64, "f16", "f16", "normal", s,
                     len_range=(1024, 65536))
+    if index == 5:
+        return Spec("ship65k", 1, 24, 4, 256, (65535,), 1, Q8_0, Q4_G32, "f16", "f16", "normal", s)
     raise ValueError(index)
 
 
-N_CONFIGS = 5
+N_CONFIGS = 6                # 0..4 the benchmark's workloads, 5 the shipped q8_0-K / q4_0-V pair
 
 
 @dataclasses.dataclass
@@ -175,6 +181,8 @@ def kv_bytes_per_token(sp: Spec) -> int:
     def row(codec):
         if codec == Q4_G64:
             return sp.head_dim // 2 + 2 * (sp.head_dim // 64)
+        if codec == Q4_G32:
+            return sp.head_dim // 2 + 2 * (sp.head_dim // 32)
         return sp.head_dim + 2 * (sp.head_dim // 32)
     return sp.n_kv_heads * (row(sp.k_codec) + row(sp.v_codec))
 
