@@ -207,13 +207,15 @@ def run_reference(args, wl, kv_bytes):
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+_CODEC_NAME = {workloads.Q4_G64: "q4_g64", workloads.Q8_0: "q8_0", workloads.Q4_G32: "q4_g32"}
+
+
 def _config(wl, args, extra=None):
     sp = wl.spec
     c = {"workload": sp.name, "n_seq": sp.n_seq, "n_heads": sp.n_heads, "n_kv_heads": sp.n_kv_heads,
          "head_dim": sp.head_dim, "kv_len": int(wl.kv_len.max()) if sp.n_seq == 1 else "ragged",
          "total_kv_tokens": int(wl.kv_len.sum()), "n_q": sp.n_q,
-         "k_codec": "q4_g64" if sp.k_codec == workloads.Q4_G64 else "q8_0",
-         "v_codec": "q4_g64" if sp.v_codec == workloads.Q4_G64 else "q8_0"}
+         "k_codec": _CODEC_NAME[sp.k_codec], "v_codec": _CODEC_NAME[sp.v_codec]}
     if extra:
         c.update(extra)
     return c

@@ -62,8 +62,13 @@ typedef enum kvq_status {
  *   FP16 scale per group, scale = fp16_rne(absmax / 127), code =
  *   clamp(rne(x / (float)scale), -127, 127); a row is head_dim code bytes plus
  *   head_dim/32 fp16 scales (8.5 bits per value).
+ * KVQ_CODEC_Q4_G32 -- the "q4_0" V cache of the shipped pair "-ctk q8_0 -ctv
+ *   q4_0" (den_llama.cpp, "What's in the fork": the q8_0-q4_0 FlashAttention
+ *   pair; "Results": the 65K serve run), whose format the pages do not give:
+ *   the Q4_G64 rule and code layout with groups of 32 values (head_dim/32
+ *   scales, 4.5 bits per value).  Not llama.cpp's q4_0 byte layout.
  * Dequantized value = (float)scale * code, exact in fp32. */
-typedef enum kvq_codec { KVQ_CODEC_Q4_G64 = 1, KVQ_CODEC_Q8_0 = 2 } kvq_codec;
+typedef enum kvq_codec { KVQ_CODEC_Q4_G64 = 1, KVQ_CODEC_Q8_0 = 2, KVQ_CODEC_Q4_G32 = 3 } kvq_codec;
 
 typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_F16 = 1 } kvq_dtype;
 

@@ -17,6 +17,7 @@ import torch
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE, KVQ_ECUDA = range(5)
 KVQ_CODEC_Q4_G64 = 1
 KVQ_CODEC_Q8_0 = 2
+KVQ_CODEC_Q4_G32 = 3
 KVQ_F32, KVQ_F16 = 0, 1
 KVQ_ERR_APPEND_POS, KVQ_ERR_KV_LEN, KVQ_ERR_TIMEOUT = 1, 2, 4
 KVQ_CAPACITY_ALIGN = 64

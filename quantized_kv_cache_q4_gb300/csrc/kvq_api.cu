@@ -29,7 +29,7 @@ kvq_status cuda_status(cudaError_t e, const char *what)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool valid_codec(int32_t c) { return c == KVQ_CODEC_Q4_G64 || c == KVQ_CODEC_Q8_0; }
+bool valid_codec(int32_t c) { return c == KVQ_CODEC_Q4_G64 || c == KVQ_CODEC_Q8_0 || c == KVQ_CODEC_Q4_G32; }
 
 bool valid_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 

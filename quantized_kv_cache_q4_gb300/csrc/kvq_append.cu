@@ -95,6 +95,27 @@ __device__ __forceinline__ int code_of(float x, float d, int qmin, int qmax)
     return q < qmin ? qmin : (q > qmax ? qmax : q);
 }
 
+// One row's share of a lane (VPL consecutive values) as 4-bit codes: the group
+// scale from the absmax over the GS / VPL lanes of the group, then the codes
+// packed two per byte (even value low nibble).
+template <int VPL, int GS>
+__device__ __forceinline__ void store_q4(const Plane &P, int64_t crow, int lane, const float (&x)[VPL], float amax)
+{
+    constexpr int D = VPL * 32;
+    constexpr int LPG = GS / VPL;                      // lanes per group
+    const __half hs = group_scale<LPG>(amax, 7.0f);
+    const float d = __half2float(hs);
+    uint64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        const uint64_t nib = (uint64_t)(code_of(x[v], d, -8, 7) & 0xF);
+        if (v < 16) lo |= nib << (4 * v);
+        else hi |= nib << (4 * (v - 16));
+    }
+    store_bytes<VPL / 2>(P.qs + crow * (D / 2) + lane * (VPL / 2), lo, hi);
+    if (lane % LPG == 0) P.sc[crow * (D / GS) + lane / LPG] = hs;
+}
+
 template <int VPL, typename SrcT>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
 {
@@ -128,18 +149,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
     const Plane P = pl ? a.plane[1] : a.plane[0];   // no dynamic index into the parameter block
     const int64_t crow = ((int64_t)s * a.n_kv_heads + h) * a.capacity + p0 + i;
     if (P.codec == KVQ_CODEC_Q4_G64) {
-        constexpr int LPG = 64 / VPL;                      // lanes per group
-        const __half hs = group_scale<LPG>(amax, 7.0f);
-        const float d = __half2float(hs);
-        uint64_t lo = 0, hi = 0;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const uint64_t nib = (uint64_t)(code_of(x[v], d, -8, 7) & 0xF);
-            if (v < 16) lo |= nib << (4 * v);
-            else hi |= nib << (4 * (v - 16));
-        }
-        store_bytes<VPL / 2>(P.qs + crow * (D / 2) + lane * (VPL / 2), lo, hi);
-        if (lane % LPG == 0) P.sc[crow * (D / 64) + lane / LPG] = hs;
+        store_q4<VPL, 64>(P, crow, lane, x, amax);
+    } else if (P.codec == KVQ_CODEC_Q4_G32) {
+        store_q4<VPL, 32>(P, crow, lane, x, amax);
     } else {
         constexpr int LPG = 32 / VPL;
         const __half hs = group_scale<LPG>(amax, 127.0f);
@@ -195,7 +207,7 @@ __global__ void dequant_kernel(Plane p, int64_t n_rows, int head_dim, float *out
     const int gs = group_size(p.codec);
     const float d = __half2float(p.sc[r * (head_dim / gs) + v0 / gs]);
     float *o = out + r * head_dim + v0;
-    if (p.codec == KVQ_CODEC_Q4_G64) {
+    if (is_q4(p.codec)) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(p.qs + r * (head_dim / 2) + v0 / 2);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {

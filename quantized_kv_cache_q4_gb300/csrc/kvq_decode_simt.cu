@@ -43,7 +43,7 @@ __device__ __forceinline__ float warp_sum(float x)
 template <int CODEC, int N>
 __device__ __forceinline__ void load_codes(const uint8_t *row, int v0, int (&c)[N])
 {
-    if constexpr (CODEC == KVQ_CODEC_Q4_G64) {
+    if constexpr (is_q4(CODEC)) {
         const uint8_t *p = row + v0 / 2;
         uint64_t w;
         if constexpr (N == 2) w = *p;
@@ -262,15 +262,27 @@ cudaError_t launch2(const DecodeArgs &a, int q_dtype, cudaStream_t st)
     }
 }
 
+template <int KC>
+cudaError_t launch_v(const DecodeArgs &a, int q_dtype, cudaStream_t st)
+{
+    switch (a.v.codec) {
+    case KVQ_CODEC_Q4_G64: return launch2<KC, KVQ_CODEC_Q4_G64>(a, q_dtype, st);
+    case KVQ_CODEC_Q8_0: return launch2<KC, KVQ_CODEC_Q8_0>(a, q_dtype, st);
+    case KVQ_CODEC_Q4_G32: return launch2<KC, KVQ_CODEC_Q4_G32>(a, q_dtype, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st)
 {
-    const bool k4 = a.k.codec == KVQ_CODEC_Q4_G64, v4 = a.v.codec == KVQ_CODEC_Q4_G64;
-    if (k4 && v4) return launch2<KVQ_CODEC_Q4_G64, KVQ_CODEC_Q4_G64>(a, q_dtype, st);
-    if (!k4 && v4) return launch2<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4_G64>(a, q_dtype, st);
-    if (k4 && !v4) return launch2<KVQ_CODEC_Q4_G64, KVQ_CODEC_Q8_0>(a, q_dtype, st);
-    return launch2<KVQ_CODEC_Q8_0, KVQ_CODEC_Q8_0>(a, q_dtype, st);
+    switch (a.k.codec) {
+    case KVQ_CODEC_Q4_G64: return launch_v<KVQ_CODEC_Q4_G64>(a, q_dtype, st);
+    case KVQ_CODEC_Q8_0: return launch_v<KVQ_CODEC_Q8_0>(a, q_dtype, st);
+    case KVQ_CODEC_Q4_G32: return launch_v<KVQ_CODEC_Q4_G32>(a, q_dtype, st);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kvq

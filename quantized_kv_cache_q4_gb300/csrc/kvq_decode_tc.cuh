@@ -1,0 +1,818 @@
+// kvq_decode_tc.cuh -- split-K decode / MTP-verify attention over a packed cache
+// on the tensor cores, for 1..32 query rows per kv head (GQA group x query
+// tokens), head_dim 64/128/256, K in Q4_G64, Q4_G32 or q8_0 and V in Q4_G64
+// or Q4_G32 (the kernel template; kvq_decode_tc.cu and kvq_decode_tc_g32.cu
+// hold its instances for the two V codecs, so that they compile in parallel)
+// (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
+// this fork is": signed INT4 + one FP16 scale per 64 values; "Results": MTP
+// n-max 2, i.e. 1 + 2 query tokens per sequence).
+//
+// Per (sequence, kv head, split) the query rows of the kv head attend to the
+// split's tokens intersected with each row's visible keys; the result is final
+// (one split) or a partial normalised over the split with its log-sum-exp.
+//
+// Work of one CTA (four warps, no dedicated producer), one CTA barrier per tile:
+//  * Thread 0 fetches the query rows with 1D bulk copies and the first tiles of
+//    64 tokens (K and V codes by swizzled 2D TMA, their fp16 scales by bulk
+//    copies) into a 3-stage shared-memory ring.  After the barrier of tile j it
+//    refills the stage of tile j - 1, which every warp has finished with.
+//  * Phase A: warp w computes S^T = K Q^T for tokens [16w, 16w+16) of the tile
+//    and all n-tiles of 8 rows on mma.sync.m16n8k16.  The K codes enter as
+//    exact fp16 integers with their bias (1032 + q or 1152 + 16 q, one LOP3 per
+//    two values); each 64-value group starts its accumulator at minus the
+//    group's bias term and is scaled by the group's fp16 scale in fp32.  The
+//    scores (log2 units) and the warp's per-row maximum go to shared memory
+//    (double-buffered by tile parity, so one barrier per tile suffices).
+//  * Phase B: every warp forms the same new running maximum from the four
+//    warps' maxima, turns the scores of its operand fragments into
+//    p = 2^(s - m) (keeping the row sums itself) and accumulates
+//    O^T += V^T P'^T for its quarter of head_dim over the tile's 64 tokens:
+//    V^T fragments from ldmatrix.trans (it pairs two tokens at one head_dim
+//    index, the A-fragment pairing), the V codes' fp16 bias taken off before
+//    the MMA (an exact fp16 subtraction: q, or 16 q at odd head_dim indices);
+//    P' = p * v_scale(token) is rounded once to fp16.  The V bias is not left
+//    for the accumulator as the K bias is: the MMA aligns its addends to the
+//    largest one and drops the bits below about 25, so 1032 * P' terms would
+//    cost the output about ten bits against a few for the scores.
+//  * Because the warps share the maximum and each owns its own columns, the
+//    end of the CTA is a division by the row sum: no cross-warp combine.
+//
+// Every mbarrier wait is bounded: after ~1 s the kernel sets KVQ_ERR_TIMEOUT in
+// the caller's error word and finishes without further waits; nothing traps.
+#pragma once
+
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+using namespace ptx;
+namespace {
+
+constexpr int kS = 3;                        // ring stages
+constexpr int kW = 4;                        // warps
+constexpr int kT = kW * 32;                  // threads
+
+__device__ __forceinline__ void warps_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kT) : "memory"); }
+
+template <int KC, int VC, int D, int NT, typename QT>
+struct TcCfg {
+    static constexpr int KRB = row_bytes(KC, D), VRB = D / 2;
+    static constexpr int KSB = 2 * scales_per_row(KC, D), VSB = 2 * scales_per_row(VC, D);
+    static constexpr int NGK = D / group_size(KC);
+    static constexpr int ROWS = NT * 8;                           // query rows kept (zero past R)
+    static constexpr int PS = ROWS + 4;                           // score row stride in floats (bank spread)
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = align_up(kTile * KRB, 1024);
+    static constexpr int KS_OFF = V_OFF + align_up(kTile * VRB, 1024);
+    static constexpr int VS_OFF = KS_OFF + align_up(kTile * KSB, 128);
+    static constexpr int STAGE = align_up(VS_OFF + kTile * VSB, 1024);
+    static constexpr int QP_OFF = kS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
+    static constexpr int KB_OFF = QP_OFF + ROWS * D * 2;          // fp32 [NGK][ROWS]: minus the K bias terms
+    // the query rows as given are only read before the first tile, the score
+    // tiles and the maxima only after it: they share one region
+    static constexpr int U_OFF = KB_OFF + align_up(ROWS * NGK * 4, 16);
+    static constexpr int QST_OFF = U_OFF;
+    static constexpr int S_OFF = U_OFF;                                   // fp32 [2][64][PS] scores
+    static constexpr int RED_OFF = S_OFF + align_up(2 * kTile * PS * 4, 16);  // fp32 [2][kW][32] maxima
+    // V scales of the tile transposed to [group][token] (0 past the split end), by tile parity
+    static constexpr int NGV = D / group_size(VC);
+    static constexpr int VT_OFF = RED_OFF + 2 * kW * 32 * 4;                  // fp16 [2][NGV][64]
+    static constexpr int QST_BYTES = ROWS * D * (int)sizeof(QT);
+    static constexpr int PR_BYTES = (VT_OFF - U_OFF) + 2 * NGV * kTile * 2;
+    static constexpr int BAR_OFF = align_up(U_OFF + (QST_BYTES > PR_BYTES ? QST_BYTES : PR_BYTES), 16);
+    static constexpr int SMEM = BAR_OFF + (kS + 1) * 8 + 1024;            // + alignment slack
+    static constexpr int MTW = (D / 64 * 4) / kW;                 // 16-row head_dim tiles per warp in phase B
+    // CTAs per SM the kernel is built for (shared memory allows 3 up to 16 rows)
+    static constexpr int MIN_BLOCKS = NT <= 2 ? 3 : 2;
+};
+
+// head_dim index fed by k-position kp (0..15) of k-step ks, in the order the K
+// unpack delivers values (Q4_G64: pairs (d, d + 4) of a 4-byte piece; q8_0:
+// pairs (d, d + 1)), and its inverse.
+template <int KC>
+__device__ __forceinline__ int kpos_to_d(int ks, int kp)
+{
+    const int hi = kp >> 3, t = (kp & 7) >> 1, h = kp & 1;
+    if constexpr (KC == KVQ_CODEC_Q4_G64) return 64 * (ks >> 2) + 32 * hi + 8 * t + (ks & 3) + 4 * h;
+    // Q4_G32: both k-steps of a group come from its one 16-byte chunk (nibble
+    // pairs 2 sub / 2 sub + 1 for the two k halves)
+    else if constexpr (KC == KVQ_CODEC_Q4_G32) return 32 * (ks >> 1) + 8 * t + 2 * (ks & 1) + hi + 4 * h;
+    else return 32 * (ks >> 1) + 16 * hi + 4 * t + 2 * (ks & 1) + h;
+}
+
+template <int KC>
+__device__ __forceinline__ int d_to_kpos(int d)
+{
+    if constexpr (KC == KVQ_CODEC_Q4_G64) {
+        const int g = d >> 6, r = d & 63, hi = r >> 5, t = (r & 31) >> 3, st = r & 3, h = (r >> 2) & 1;
+        return 16 * (4 * g + st) + 8 * hi + 2 * t + h;
+    } else if constexpr (KC == KVQ_CODEC_Q4_G32) {
+        const int g = d >> 5, t = (d & 31) >> 3, w = d & 7, h = w >> 2, sub = (w >> 1) & 1, hi = w & 1;
+        return 16 * (2 * g + sub) + 8 * hi + 2 * t + h;
+    } else {
+        const int g = d >> 5, r = d & 31, hi = r >> 4, t = (r & 15) >> 2, st = (r >> 1) & 1, h = r & 1;
+        return 16 * (2 * g + st) + 8 * hi + 2 * t + h;
+    }
+}
+
+// byte offset of 16-byte chunk c of row n of the permuted query copy (D halves a row)
+template <int D>
+__device__ __forceinline__ uint32_t qp_chunk_off(int n, int c)
+{
+    return (uint32_t)(n * D * 2 + ((c ^ (n & 7)) << 4));
+}
+
+// Nibble pair e (0..3) of a code word as fp16x2 with its bias left in: pair e
+// holds nibbles e and e + 4 (the order the ldmatrix.trans fragment pairs two
+// tokens in), as 1032 + q for even e and 1152 + 16 q for odd e.
+__device__ __forceinline__ uint32_t q4_pair_biased(uint32_t w, int e)
+{
+    const uint32_t x = (e & 2) ? (w >> 8) : w;
+    return (e & 1) ? lop3_ac(x, 0x64806480u, 0x64706470u) : lop3_ac(x, 0x64086408u, 0x64076407u);
+}
+
+// The same pair without its bias: q for even e, 16 q for odd e (an exact fp16
+// subtraction of 1032 = 0x6408 or 1152 = 0x6480).
+__device__ __forceinline__ uint32_t q4_pair(uint32_t w, int e)
+{
+    const uint32_t b = q4_pair_biased(w, e);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"((e & 1) ? 0x64806480u : 0x64086408u));
+    return r;
+}
+
+// The query rows as fp16, head_dim permuted to the K-unpack order and swizzled
+// for ldmatrix ([ROWS][D], rows >= R zero); with Q4_G64 K the odd head_dim
+// indices are divided by 16 (exact for normal values) because their codes
+// arrive as 1152 + 16 q.  Each thread builds whole 16-byte chunks (8
+// k-positions of one k-step, so of one K group); the CPG chunks of a group sit
+// in consecutive lanes, whose shuffle sum gives minus the group's bias term
+// sum_d bias(d) q(d) (bias 1032 at even, 1152 at odd d for Q4_G64; 1152 for
+// q8_0) in kb_s[group][row].
+template <int KC, int D, int ROWS, typename QT>
+__device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb_s, int R, bool ok)
+{
+    constexpr int CPR = D / 8;                     // chunks per row
+    constexpr int CPG = group_size(KC) / 8;        // chunks per K group
+    for (int ci = threadIdx.x; ci < ROWS * CPR; ci += kT) {    // whole warps per step
+        const int n = ci / CPR, c = ci % CPR;
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int kg = 8 * c + j;
+            const int d = kpos_to_d<KC>(kg >> 4, kg & 15);
+            x[j] = 0.0f;
+            if (n < R && ok) {
+                if constexpr (sizeof(QT) == 2) x[j] = __half2float(qst[n * D + d]);
+                else x[j] = __half2float(__float2half_rn(qst[n * D + d]));
+            }
+            if constexpr (is_q4(KC))
+                if (d & 1) x[j] *= 0.0625f;
+        }
+        uint32_t hw[4];
+        float b = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hw[j] = pack_f16x2(x[2 * j], x[2 * j + 1]);
+            const float2 hf = __half22float2(u32_as_h2(hw[j]));
+            // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
+            const int kg = 8 * c + 2 * j;
+            const bool even = is_q4(KC) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
+            b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
+        }
+        *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+#pragma unroll
+        for (int off = 1; off < CPG; off <<= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
+        if (c % CPG == 0) kb_s[(c / CPG) * ROWS + n] = -b;
+    }
+}
+
+template <typename C, typename KG, typename VG>
+__device__ __forceinline__ void issue_tile(uint32_t base, uint32_t full, const CUtensorMap *tmk,
+                                           const CUtensorMap *tmv, const uint8_t *ksc, const uint8_t *vsc,
+                                           int64_t row0)
+{
+    // the cache is read once per call: evict-first in L2
+    const uint64_t pol = evict_first_policy();
+    mbar_expect_tx(full, (uint32_t)(KG::BYTES + VG::BYTES + kTile * (C::KSB + C::VSB)));
+    const int y = (int)row0;
+#pragma unroll
+    for (int b = 0; b < KG::NB; ++b)
+        tma_load_2d(base + C::K_OFF + b * kTile * KG::BI, tmk, b * KG::BI, y, full, pol);
+#pragma unroll
+    for (int b = 0; b < VG::NB; ++b)
+        tma_load_2d(base + C::V_OFF + b * kTile * VG::BI, tmv, b * VG::BI, y, full, pol);
+    bulk_load_hint(base + C::KS_OFF, ksc + row0 * C::KSB, kTile * C::KSB, full, pol);
+    bulk_load_hint(base + C::VS_OFF, vsc + row0 * C::VSB, kTile * C::VSB, full, pol);
+}
+
+template <int KC, int VC, int D, int NT, typename QT>
+__global__ void __launch_bounds__(kT, (TcCfg<KC, VC, D, NT, QT>::MIN_BLOCKS))
+decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
+{
+    using C = TcCfg<KC, VC, D, NT, QT>;
+    using KG = TileGeom<C::KRB>;
+    using VG = TileGeom<C::VRB>;
+    constexpr int NGK = C::NGK;
+    constexpr int KSTEP_PER_G = group_size(KC) / 16;
+    constexpr int MTW = C::MTW;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qp = smem + C::QP_OFF;
+    float *kb_s = reinterpret_cast<float *>(smem + C::KB_OFF);
+    float *s_s0 = reinterpret_cast<float *>(smem + C::S_OFF);        // [2][64][PS]
+    float *red_m0 = reinterpret_cast<float *>(smem + C::RED_OFF);    // [2][kW][32]
+    __half *vt0 = reinterpret_cast<__half *>(smem + C::VT_OFF);      // [2][NGV][64]
+    const uint32_t bar_full = smem_u32(smem + C::BAR_OFF);
+    const uint32_t bar_q = bar_full + kS * 8;
+    __shared__ volatile int s_timeout;
+    __shared__ int s_issued;
+
+    const int split = blockIdx.x, kh = blockIdx.y;
+    __shared__ int s_seq;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int R = a.n_q * G;                             // <= 8 * NT
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+        s_timeout = 0;
+        s_issued = 0;
+        for (int i = 0; i < kS; ++i) mbar_init(bar_full + 8 * i, 1);
+        mbar_init(bar_q, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait();
+    // The grid's z index is a rank: sequences in order of decreasing length, so
+    // the CTAs of the longest sequences of a ragged batch are dispatched first
+    // (a longest-first schedule).  Ties go by index; identity beyond kT sequences.
+    int s = blockIdx.z;
+    if (a.n_seq > 1 && a.n_seq <= kT) {
+        if ((int)threadIdx.x < a.n_seq) {
+            const int t = threadIdx.x, lt = a.kv_len[t];
+            int rank = 0;
+            for (int u = 0; u < a.n_seq; ++u) {
+                const int lu = a.kv_len[u];
+                rank += (lu > lt) || (lu == lt && u < t);
+            }
+            if (rank == (int)blockIdx.z) s_seq = t;
+        }
+        __syncthreads();
+        s = s_seq;
+    }
+    // query rows (for each query token, the G heads of this kv head are one
+    // contiguous run) by bulk copy, in parallel with what follows
+    if (threadIdx.x == 0) {
+        const uint32_t run = (uint32_t)(G * D * sizeof(QT));
+        mbar_expect_tx(bar_q, run * (uint32_t)a.n_q);
+        const QT *q = static_cast<const QT *>(a.q);
+        for (int i = 0; i < a.n_q; ++i)
+            bulk_load(smem_u32(smem + C::QST_OFF) + i * run, q + (((int64_t)s * a.n_q + i) * a.n_heads + kh * G) * D,
+                      run, bar_q);
+    }
+
+    int len = a.kv_len[s];
+    if (len < 0 || len > a.max_kv_len) {
+        if (threadIdx.x == 0 && split == 0 && kh == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
+        len = len < 0 ? 0 : a.max_kv_len;
+    }
+    int lo, hi;
+    split_range(len, a.n_splits, split, lo, hi);
+    const int n_tiles = (int)ceil_div(hi - lo, kTile);
+    const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
+    const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
+    const uint8_t *vsc = reinterpret_cast<const uint8_t *>(a.v.sc);
+    if (threadIdx.x == 0) {
+        const int first = min(kS, n_tiles);
+        for (int j = 0; j < first; ++j)
+            issue_tile<C, KG, VG>(smem_u32(smem + j * C::STAGE), bar_full + 8 * j, &tmk, &tmv, ksc, vsc,
+                                  plane_row + lo + j * kTile);
+        s_issued = first;
+    }
+
+    // the query rows, permuted and swizzled, and the K bias terms
+    if (!mbar_wait(bar_q, 0)) s_timeout = 1;
+    prep_query<KC, D, C::ROWS>(reinterpret_cast<const QT *>(smem + C::QST_OFF), qp, kb_s, R, !s_timeout);
+    __syncthreads();
+
+    int nv[NT][2];
+    int nv_min = 0x7FFFFFFF;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int r = nt * 8 + 2 * tig + c;
+            nv[nt][c] = r < R ? len - a.n_q + r / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
+            nv_min = min(nv_min, nv[nt][c]);
+        }
+    const float sl2 = a.scale_log2;
+    const int tl = warp * 16;                                           // phase A tokens
+    // K fragments: one ldmatrix.x4 per 32 bytes of a token row (two 16-byte
+    // chunks: one group of Q4_G64 or q8_0, two groups of Q4_G32)
+    constexpr int NLU = C::KRB / 32;
+    constexpr int GPU = (KC == KVQ_CODEC_Q4_G32) ? 2 : 1;          // K groups per ldmatrix
+    uint32_t koff[NLU];
+    {
+        const int ktok = tl + (lane & 7) + 8 * ((lane >> 3) & 1), kch = lane >> 4;
+#pragma unroll
+        for (int u = 0; u < NLU; ++u) koff[u] = KG::chunk_addr(C::K_OFF, ktok, 2 * u + kch);
+    }
+    // Phase B head_dim slice: 16-row tiles mt = warp * MTW + t; tile mt covers
+    // the 16-byte V chunk mt / 2 (32 head_dim values), its rows 0-7 the nibble
+    // pair 2 (mt % 2) (even head_dim index), rows 8-15 the pair 2 (mt % 2) + 1
+    // (odd index), so a tile never spans two V groups.  The warp's tiles lie in
+    // chunks cw and cw1 (= cw when it has at most two tiles).
+    const int cw = (warp * MTW) >> 1, cw1 = (MTW == 4) ? cw + 1 : cw;
+    constexpr int NGW = (MTW == 4 && VC == KVQ_CODEC_Q4_G32) ? 2 : 1;   // V groups a warp's tiles touch
+    const int gv0 = (32 * cw) / group_size(VC);                          // the first of them
+    const uint32_t voff0 =
+        VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), ((lane >> 3) & 1) ? cw1 : cw);
+    const uint32_t qp_base = smem_u32(qp);
+    // with one n-tile the query's B fragments fit in registers for the whole CTA
+    constexpr bool QREG = (NT == 1);
+    constexpr int KSTEPS = D / 16;
+    uint32_t qf[QREG ? KSTEPS : 1][2];
+    if constexpr (QREG) {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+            ldsm_x2(qp_base + qp_chunk_off<D>(lane & 7, 2 * ks + ((lane >> 3) & 1)), qf[ks][0], qf[ks][1]);
+    }
+
+    float o[MTW][NT][4];
+#pragma unroll
+    for (int t = 0; t < MTW; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[t][nt][c] = 0.0f;
+    // running maximum and (partial) sum of row nt * 8 + gid, the row this lane's
+    // phase-B operand fragments belong to; every warp holds the same maxima
+    float mg[NT], lg[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mg[nt] = -INFINITY, lg[nt] = 0.0f;
+
+    // ---- phase A of tile jj: S^T for this warp's 16 tokens (log2 units, not yet
+    // masked) and the tile's V scales transposed for phase B (0 past the split end)
+    auto phase_a = [&](int jj, float (&sc)[NT][4]) {
+        const int st = jj % kS;
+        const int tb = lo + jj * kTile + tl;
+        const uint32_t base = smem_u32(smem + st * C::STAGE);
+        const uint8_t *ksp = smem + st * C::STAGE + C::KS_OFF;
+        const uint8_t *vsp = smem + st * C::STAGE + C::VS_OFF;
+        __half *vt = vt0 + (jj & 1) * (C::NGV * kTile);
+        for (int i = lane; i < 16 * C::NGV; i += 32) {
+            const int t = i & 15, g = i >> 4;
+            vt[g * kTile + tl + t] =
+                (tb + t < hi) ? reinterpret_cast<const __half *>(vsp + (tl + t) * C::VSB)[g] : __float2half_rn(0.0f);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[nt][c] = 0.0f;
+        float sk0[NGK], sk1[NGK];
+        load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
+        load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
+#pragma unroll
+        for (int u = 0; u < NLU; ++u) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(base + koff[u], r0, r1, r2, r3);
+            uint32_t h0[4], h1[4], h2[4], h3[4];
+            if constexpr (is_q4(KC)) {
+                unpack_q4_biased(r0, h0);
+                unpack_q4_biased(r1, h1);
+                unpack_q4_biased(r2, h2);
+                unpack_q4_biased(r3, h3);
+            } else {
+                uint32_t t2[2];
+                unpack_q8_biased(r0, t2); h0[0] = t2[0]; h0[1] = t2[1];
+                unpack_q8_biased(r1, t2); h1[0] = t2[0]; h1[1] = t2[1];
+                unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
+                unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
+            }
+#pragma unroll
+            for (int gi = 0; gi < GPU; ++gi) {
+                const int g = u * GPU + gi;
+                // each group's accumulator starts at minus its bias term (the first
+                // k-step's MMA takes it as its accumulator input)
+                float cg[NT][4];
+                float2 nb2[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    nb2[nt] = *reinterpret_cast<const float2 *>(kb_s + g * C::ROWS + nt * 8 + 2 * tig);
+#pragma unroll
+                for (int k = 0; k < KSTEP_PER_G; ++k) {
+                    const int ks = g * KSTEP_PER_G + k;
+                    // A fragment: Q4_G32 takes both k halves from the group's own chunk
+                    // (nibble pairs 2k and 2k + 1); the others take k half 0 from the
+                    // first chunk and half 1 from the second
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (KC == KVQ_CODEC_Q4_G32) {
+                        a0 = gi ? h2[2 * k] : h0[2 * k];
+                        a1 = gi ? h3[2 * k] : h1[2 * k];
+                        a2 = gi ? h2[2 * k + 1] : h0[2 * k + 1];
+                        a3 = gi ? h3[2 * k + 1] : h1[2 * k + 1];
+                    } else {
+                        a0 = h0[k];
+                        a1 = h1[k];
+                        a2 = h2[k];
+                        a3 = h3[k];
+                    }
+#pragma unroll
+                    for (int np = 0; np < (NT + 1) / 2; ++np) {
+                        // B fragments of n-tiles 2np and 2np+1 (the second exists only
+                        // when 2np + 1 < NT)
+                        uint32_t b00, b01, b10, b11;
+                        if constexpr (QREG) {
+                            b00 = qf[ks][0];
+                            b01 = qf[ks][1];
+                            b10 = b11 = 0u;
+                        } else if (2 * np + 1 < NT) {
+                            const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
+                            ldsm_x4(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10, b11);
+                        } else {
+                            const int qrow = 2 * np * 8 + (lane & 7);
+                            ldsm_x2(qp_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
+                            b10 = b11 = 0u;
+                        }
+                        if (k == 0) {
+                            const float2 c = nb2[2 * np];
+                            mma16816_c(cg[2 * np], a0, a1, a2, a3, b00, b01, c.x, c.y, c.x, c.y);
+                            if (2 * np + 1 < NT) {
+                                const float2 c1 = nb2[2 * np + 1];
+                                mma16816_c(cg[2 * np + 1], a0, a1, a2, a3, b10, b11, c1.x, c1.y, c1.x, c1.y);
+                            }
+                        } else {
+                            mma16816(cg[2 * np], a0, a1, a2, a3, b00, b01);
+                            if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], a0, a1, a2, a3, b10, b11);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    sc[nt][0] = fmaf(cg[nt][0], sk0[g], sc[nt][0]);
+                    sc[nt][1] = fmaf(cg[nt][1], sk0[g], sc[nt][1]);
+                    sc[nt][2] = fmaf(cg[nt][2], sk1[g], sc[nt][2]);
+                    sc[nt][3] = fmaf(cg[nt][3], sk1[g], sc[nt][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[nt][c] *= sl2;
+    };
+
+    // ---- end of phase A: mask (split end, causal rows), store the scores and
+    // this warp's per-row maximum of the tile for phase B
+    auto phase_a_store = [&](int jj, float (&sc)[NT][4]) {
+        const int tb = lo + jj * kTile + tl;
+        const int ta = tb + gid, tc = ta + 8;
+        if (tb + 16 > hi || tb + 16 > nv_min) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (!(ta < hi && ta < nv[nt][0])) sc[nt][0] = -INFINITY;
+                if (!(ta < hi && ta < nv[nt][1])) sc[nt][1] = -INFINITY;
+                if (!(tc < hi && tc < nv[nt][0])) sc[nt][2] = -INFINITY;
+                if (!(tc < hi && tc < nv[nt][1])) sc[nt][3] = -INFINITY;
+            }
+        }
+        float *s_s = s_s0 + (jj & 1) * (kTile * C::PS);
+        float *red_m = red_m0 + (jj & 1) * (kW * 32);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            *reinterpret_cast<float2 *>(s_s + (tl + gid) * C::PS + nt * 8 + 2 * tig) = make_float2(sc[nt][0], sc[nt][1]);
+            *reinterpret_cast<float2 *>(s_s + (tl + gid + 8) * C::PS + nt * 8 + 2 * tig) =
+                make_float2(sc[nt][2], sc[nt][3]);
+            float mx0 = fmaxf(sc[nt][0], sc[nt][2]), mx1 = fmaxf(sc[nt][1], sc[nt][3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            if (gid == 0) *reinterpret_cast<float2 *>(red_m + warp * 32 + nt * 8 + 2 * tig) = make_float2(mx0, mx1);
+        }
+    };
+
+    // ---- phase B of tile jj: softmax of the tile and O^T += V^T P'^T for this
+    // warp's head_dim slice
+    auto phase_b = [&](int jj) {
+        const int st = jj % kS;
+        const uint32_t base = smem_u32(smem + st * C::STAGE);
+        const float *s_s = s_s0 + (jj & 1) * (kTile * C::PS);
+        const float *red_m = red_m0 + (jj & 1) * (kW * 32);
+        const __half *vt = vt0 + (jj & 1) * (C::NGV * kTile);
+        // new running maximum of row nt * 8 + gid (the same in every warp)
+        float cf[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int r = nt * 8 + gid;
+            float tmax = red_m[r];
+#pragma unroll
+            for (int w = 1; w < kW; ++w) tmax = fmaxf(tmax, red_m[w * 32 + r]);
+            const float mn = fmaxf(mg[nt], tmax);
+            cf[nt] = (mn == -INFINITY) ? 1.0f : ex2(mg[nt] - mn);
+            mg[nt] = mn;
+            lg[nt] *= cf[nt];
+        }
+        // accumulator columns are rows 2 tig and 2 tig + 1: their factors come from
+        // the lanes whose fragment row they are (1 unless the maximum grew)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float c0 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig);
+            const float c1 = __shfl_sync(0xffffffffu, cf[nt], 8 * tig + 4);
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+                o[t][nt][0] *= c0;
+                o[t][nt][1] *= c1;
+                o[t][nt][2] *= c0;
+                o[t][nt][3] *= c1;
+            }
+        }
+        float msub[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+            // tokens past the split end have score -inf (p = 0) and V scale 0
+            uint32_t r0, r1, r2, r3;           // tokens 0-7 / 8-15 of chunks cw and cw1
+            ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
+            float p[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float *sr = s_s + (16 * kk + 2 * tig) * C::PS + nt * 8 + gid;
+                p[nt][0] = ex2(sr[0] - msub[nt]);
+                p[nt][1] = ex2(sr[C::PS] - msub[nt]);
+                p[nt][2] = ex2(sr[8 * C::PS] - msub[nt]);
+                p[nt][3] = ex2(sr[9 * C::PS] - msub[nt]);
+                lg[nt] += (p[nt][0] + p[nt][1]) + (p[nt][2] + p[nt][3]);
+            }
+            // P' = p * v_scale(token, group), one B fragment set per V group
+            uint32_t b0[NGW][NT], b1[NGW][NT];
+#pragma unroll
+            for (int q = 0; q < NGW; ++q) {
+                const __half *vq = vt + (gv0 + q) * kTile + 16 * kk + 2 * tig;
+                const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(vq));
+                const float2 s89 = __half22float2(*reinterpret_cast<const __half2 *>(vq + 8));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    b0[q][nt] = pack_f16x2(p[nt][0] * s01.x, p[nt][1] * s01.y);
+                    b1[q][nt] = pack_f16x2(p[nt][2] * s89.x, p[nt][3] * s89.y);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < MTW; ++t) {
+                // tile t: chunk cw + lc, nibble pairs 2j (rows 0-7) and 2j + 1 (rows 8-15)
+                const int lc = (MTW >= 2) ? (t >> 1) : 0;
+                const int j = (MTW >= 2) ? (t & 1) : (warp & 1);
+                const int q = (NGW == 2) ? lc : 0;
+                const uint32_t ra = lc ? r1 : r0, rb = lc ? r3 : r2;
+                const uint32_t a0 = q4_pair(ra, 2 * j), a1 = q4_pair(ra, 2 * j + 1);
+                const uint32_t a2 = q4_pair(rb, 2 * j), a3 = q4_pair(rb, 2 * j + 1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[q][nt], b1[q][nt]);
+            }
+        }
+    };
+
+    if constexpr (NT == 1) {
+        // Software-pipelined tile loop: iteration j runs phase A of tile j + 1 and
+        // phase B of tile j, two independent instruction streams in one block (the
+        // scores, maxima and transposed V scales are double-buffered by tile
+        // parity), then the one CTA barrier, which also orders every warp's reads
+        // of tile j before its stage is refilled with tile j + kS.  The last
+        // tile's phase B runs alone.  After a timeout the waits are skipped and
+        // the warps keep stepping over stale data (the result is flagged as
+        // invalid), so every warp reaches every barrier.
+        if (n_tiles > 0) {
+            if (!s_timeout && !mbar_wait(bar_full, 0)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(0, sc);
+            phase_a_store(0, sc);
+        }
+        warps_sync();
+        for (int j = 0; j + 1 < n_tiles; ++j) {
+            if (!s_timeout && !mbar_wait(bar_full + 8 * ((j + 1) % kS), ((j + 1) / kS) & 1)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(j + 1, sc);
+            phase_b(j);
+            phase_a_store(j + 1, sc);
+            warps_sync();
+            if (threadIdx.x == 0 && !s_timeout && j + kS < n_tiles) {
+                issue_tile<C, KG, VG>(smem_u32(smem + (j % kS) * C::STAGE), bar_full + 8 * (j % kS), &tmk, &tmv, ksc,
+                                      vsc, plane_row + lo + (j + kS) * kTile);
+                s_issued = j + kS + 1;
+            }
+        }
+        if (n_tiles > 0) phase_b(n_tiles - 1);
+    } else {
+        // Several n-tiles: registers do not allow both phases at once.  Per tile:
+        // phase A, the one CTA barrier (which also orders every warp's reads of
+        // tile j - 1 before that stage is refilled with tile j - 1 + kS), phase B.
+        for (int j = 0; j < n_tiles; ++j) {
+            if (!s_timeout && !mbar_wait(bar_full + 8 * (j % kS), (j / kS) & 1)) s_timeout = 1;
+            float sc[NT][4];
+            phase_a(j, sc);
+            phase_a_store(j, sc);
+            warps_sync();
+            if (threadIdx.x == 0 && j >= 1 && !s_timeout && j - 1 + kS < n_tiles) {
+                issue_tile<C, KG, VG>(smem_u32(smem + ((j - 1) % kS) * C::STAGE), bar_full + 8 * ((j - 1) % kS), &tmk,
+                                      &tmv, ksc, vsc, plane_row + lo + (j - 1 + kS) * kTile);
+                s_issued = j - 1 + kS + 1;
+            }
+            phase_b(j);
+        }
+    }
+    // the dependent launch (the merge of the splits) may start now: its CTAs
+    // find the SMs that finishing CTAs of this grid leave free
+    pdl_trigger();
+
+    // row sums: each lane summed a quarter of the tokens of its fragment row
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        lg[nt] += __shfl_xor_sync(0xffffffffu, lg[nt], 1);
+        lg[nt] += __shfl_xor_sync(0xffffffffu, lg[nt], 2);
+    }
+    // never leave while a copy into this CTA's shared memory could be in flight
+    // (only possible after a timeout; otherwise every issued copy was waited on)
+    if (threadIdx.x == 0 && s_timeout) {
+        const int issued = s_issued;
+        for (int j = issued - 1; j >= 0 && j >= issued - kS; --j) mbar_wait(bar_full + 8 * (j % kS), (j / kS) & 1);
+        mbar_wait(bar_q, 0);
+    }
+    const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int cl = 0; cl < 2; ++cl) {
+            // accumulator column 2 tig + cl (elements cl and cl + 2 of a tile): its sum
+            // and maximum sit in the lanes whose fragment row it is
+            const float L = __shfl_sync(0xffffffffu, lg[nt], 8 * tig + 4 * cl);
+            const float M = __shfl_sync(0xffffffffu, mg[nt], 8 * tig + 4 * cl);
+            const int n = nt * 8 + 2 * tig + cl;
+            if (n >= R) continue;
+            const bool empty = (M == -INFINITY || L <= 0.0f);
+            const float inv = empty ? 0.0f : 1.0f / L;
+            // rows of odd head_dim index were accumulated 16x (their codes' 1152 + 16 q form)
+            const float inv16 = inv * 0.0625f;
+            const int i = n / G, jj = n % G;
+            const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
+            float *dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
+            if constexpr (MTW >= 2) {
+                // tiles 2 lc and 2 lc + 1 fill head_dim 32 (cw + lc) + 4 gid + 0..3
+#pragma unroll
+                for (int lc = 0; lc < MTW / 2; ++lc)
+                    *reinterpret_cast<float4 *>(dst + 32 * (cw + lc) + 4 * gid) =
+                        make_float4(o[2 * lc][nt][cl] * inv, o[2 * lc][nt][cl + 2] * inv16,
+                                    o[2 * lc + 1][nt][cl] * inv, o[2 * lc + 1][nt][cl + 2] * inv16);
+            } else {
+                *reinterpret_cast<float2 *>(dst + 32 * cw + 4 * gid + 2 * (warp & 1)) =
+                    make_float2(o[0][nt][cl] * inv, o[0][nt][cl + 2] * inv16);
+            }
+            if (warp == 0 && gid == 0) {
+                const float lse = empty ? -INFINITY : (M + log2f(L)) * kLn2;
+                if (a.n_splits == 1) {
+                    if (a.out_lse) a.out_lse[orow] = lse;
+                } else {
+                    a.part_lse[(int64_t)split * rows_total + orow] = lse;
+                }
+            }
+        }
+    if (threadIdx.x == 0 && s_timeout && a.err) atomicOr(a.err, KVQ_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+// Kernel attributes (dynamic shared memory, carveout), set once per device, and
+// the CTAs per SM they allow.
+template <typename C, typename Kern>
+cudaError_t prepare_kernel(Kern kern, int *per_sm)
+{
+    static int resident[64] = {};            // per device; 0 = not prepared yet
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && resident[dev] > 0) {
+        *per_sm = resident[dev];
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kT, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) resident[dev] = n;
+    *per_sm = n;
+    return cudaSuccess;
+}
+
+template <typename C, typename Kern>
+cudaError_t launch_cfg(Kern kern, const DecodeArgs &a, cudaStream_t st)
+{
+    static_assert(C::SMEM <= 227 * 1024, "shared memory of one CTA");
+    const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
+    CUtensorMap tk, tv;
+    if (!make_codes_map(&tk, a.k.qs, C::KRB, rows) || !make_codes_map(&tv, a.v.qs, C::VRB, rows))
+        return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaError_t e = prepare_kernel<C>(kern, &per_sm);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
+    return launch_pdl(kern, grid, dim3(kT), C::SMEM, st, a, tk, tv);
+}
+
+template <int KC, int VC, int D>
+int per_sm_nt(int nt)
+{
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (nt) {
+    case 1: e = prepare_kernel<TcCfg<KC, VC, D, 1, __half>>(decode_tc_kernel<KC, VC, D, 1, __half>, &n); break;
+    case 2: e = prepare_kernel<TcCfg<KC, VC, D, 2, __half>>(decode_tc_kernel<KC, VC, D, 2, __half>, &n); break;
+    case 3: e = prepare_kernel<TcCfg<KC, VC, D, 3, __half>>(decode_tc_kernel<KC, VC, D, 3, __half>, &n); break;
+    case 4: e = prepare_kernel<TcCfg<KC, VC, D, 4, __half>>(decode_tc_kernel<KC, VC, D, 4, __half>, &n); break;
+    default: break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int KC, int VC>
+int per_sm_d(int head_dim, int nt)
+{
+    switch (head_dim) {
+    case 64: return per_sm_nt<KC, VC, 64>(nt);
+    case 128: return per_sm_nt<KC, VC, 128>(nt);
+    case 256: return per_sm_nt<KC, VC, 256>(nt);
+    default: return 0;
+    }
+}
+
+template <int KC, int VC, int D, int NT, typename QT>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st)
+{
+    return launch_cfg<TcCfg<KC, VC, D, NT, QT>>(decode_tc_kernel<KC, VC, D, NT, QT>, a, st);
+}
+
+template <int KC, int VC, int D, typename QT>
+cudaError_t launch_nt(const DecodeArgs &a, cudaStream_t st)
+{
+    const int R = a.n_q * (a.n_heads / a.n_kv_heads);
+    switch ((R + 7) / 8) {
+    case 1: return launch_t<KC, VC, D, 1, QT>(a, st);
+    case 2: return launch_t<KC, VC, D, 2, QT>(a, st);
+    case 3: return launch_t<KC, VC, D, 3, QT>(a, st);
+    case 4: return launch_t<KC, VC, D, 4, QT>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int KC, int VC, typename QT>
+cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st)
+{
+    switch (a.head_dim) {
+    case 64: return launch_nt<KC, VC, 64, QT>(a, st);
+    case 128: return launch_nt<KC, VC, 128, QT>(a, st);
+    case 256: return launch_nt<KC, VC, 256, QT>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int VC, typename QT>
+cudaError_t launch_k(const DecodeArgs &a, cudaStream_t st)
+{
+    switch (a.k.codec) {
+    case KVQ_CODEC_Q4_G64: return launch_d<KVQ_CODEC_Q4_G64, VC, QT>(a, st);
+    case KVQ_CODEC_Q8_0: return launch_d<KVQ_CODEC_Q8_0, VC, QT>(a, st);
+    case KVQ_CODEC_Q4_G32: return launch_d<KVQ_CODEC_Q4_G32, VC, QT>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// The kernel for V in codec VC: launch, and CTAs per SM for a K codec.
+template <int VC>
+cudaError_t launch_for_v(const DecodeArgs &a, int q_dtype, cudaStream_t st)
+{
+    return q_dtype == KVQ_F16 ? launch_k<VC, __half>(a, st) : launch_k<VC, float>(a, st);
+}
+
+template <int VC>
+int per_sm_for_v(int k_codec, int head_dim, int nt)
+{
+    switch (k_codec) {
+    case KVQ_CODEC_Q4_G64: return per_sm_d<KVQ_CODEC_Q4_G64, VC>(head_dim, nt);
+    case KVQ_CODEC_Q8_0: return per_sm_d<KVQ_CODEC_Q8_0, VC>(head_dim, nt);
+    case KVQ_CODEC_Q4_G32: return per_sm_d<KVQ_CODEC_Q4_G32, VC>(head_dim, nt);
+    default: return 0;
+    }
+}
+
+}  // namespace
+}  // namespace kvq

@@ -16,8 +16,10 @@ constexpr int kWarp = 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// 4-bit codecs (Q4_G64, Q4_G32) share the code layout; q8_0 has one byte per value.
+__host__ __device__ constexpr bool is_q4(int codec) { return codec == KVQ_CODEC_Q4_G64 || codec == KVQ_CODEC_Q4_G32; }
 __host__ __device__ constexpr int group_size(int codec) { return codec == KVQ_CODEC_Q4_G64 ? 64 : 32; }
-__host__ __device__ constexpr int row_bytes(int codec, int d) { return codec == KVQ_CODEC_Q4_G64 ? d / 2 : d; }
+__host__ __device__ constexpr int row_bytes(int codec, int d) { return is_q4(codec) ? d / 2 : d; }
 __host__ __device__ constexpr int scales_per_row(int codec, int d) { return d / group_size(codec); }
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -91,12 +93,15 @@ void set_last_error(const char *msg);
 
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);
-// Tensor-core path: 1..32 query rows per kv head, head_dim 64/128/256, V in Q4_G64.
+// Tensor-core path: 1..32 query rows per kv head, head_dim 64/128/256, V in Q4_G64 or Q4_G32.
 bool decode_tc_supported(const DecodeArgs &a);
 cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // CTAs of the tensor-core decode kernel that fit on one SM for these caches and
 // query rows per kv head; 0 if that kernel does not take them or no device answers.
 int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_head);
+// The same kernel for V in Q4_G32 (its own translation unit).
+cudaError_t launch_decode_tc_g32(const DecodeArgs &a, int q_dtype, cudaStream_t st);
+int decode_tc_g32_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int rows, int head_dim,
                          float *out, float *out_lse, cudaStream_t st);
 cudaError_t launch_dequant(const Plane &p, int64_t n_rows, int head_dim, float *out, cudaStream_t st);

@@ -60,7 +60,8 @@ def test_split_counts(n_splits):
 
 
 @pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0),
-                                   (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0)])
+                                   (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32),
+                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32), (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0)])
 @pytest.mark.parametrize("D", [128, 256, 512])
 def test_codec_pairs(kc, vc, D):
     wl = workloads.custom(n_seq=2, n_heads=8, n_kv_heads=2, head_dim=D, cached=(700, 333), n_new=1, k_codec=kc,
@@ -69,6 +70,24 @@ def test_codec_pairs(kc, vc, D):
     o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
     for n_splits in (1, 5):
         o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("kc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32])
+@pytest.mark.parametrize("vc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G32])
+@pytest.mark.parametrize("G,n_new", [(1, 1), (6, 3), (8, 4)])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
+    """Every K codec with both 4-bit V codecs, at 1..32 query rows per kv head
+    (one to four 8-row n-tiles) and a ragged last tile."""
+    wl = workloads.custom(n_seq=2, n_heads=2 * G, n_kv_heads=2, head_dim=D, cached=(900 - n_new, 161), n_new=n_new,
+                          k_codec=kc, v_codec=vc, src_dtype="f16", q_dtype="f16", dist="outliers",
+                          seed=11 * kc + 5 * vc + G + D)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (0, 3):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
         check_close(o, o_ref, lse, lse_ref)
 
 
