@@ -28,12 +28,16 @@
 //    p = 2^(s - m) (keeping the row sums itself) and accumulates
 //    O^T += V^T P'^T for its quarter of head_dim over the tile's 64 tokens:
 //    V^T fragments from ldmatrix.trans (it pairs two tokens at one head_dim
-//    index, the A-fragment pairing), the V codes' fp16 bias taken off before
-//    the MMA (an exact fp16 subtraction: q, or 16 q at odd head_dim indices);
-//    P' = p * v_scale(token) is rounded once to fp16.  The V bias is not left
-//    for the accumulator as the K bias is: the MMA aligns its addends to the
-//    largest one and drops the bits below about 25, so 1032 * P' terms would
-//    cost the output about ten bits against a few for the scores.
+//    index, the A-fragment pairing); P' = p * v_scale(token) is rounded once
+//    to fp16.  With one n-tile and one V group per warp the V codes enter as
+//    exact fp16 subnormals (q + 8) 2^-24 (16 (q + 8) 2^-24 at odd head_dim
+//    indices), one LOP3 per two values, and their offset 8 is removed once per
+//    tile from the tile's sum of P' (one MMA against a ones operand per 16
+//    tokens); otherwise, where that sum would take one MMA per n-tile and V
+//    group, an exact fp16 subtraction turns the biased form into q (16 q).
+//    The V offset is kept small, unlike the K bias: the MMA aligns its
+//    addends to the largest one and drops the bits below about 25, so
+//    1032 * P' terms would cost the output about ten bits.
 //  * Because the warps share the maximum and each owns its own columns, the
 //    end of the CTA is a division by the row sum: no cross-warp combine.
 //
@@ -130,8 +134,17 @@ __device__ __forceinline__ uint32_t q4_pair_biased(uint32_t w, int e)
     return (e & 1) ? lop3_ac(x, 0x64806480u, 0x64706470u) : lop3_ac(x, 0x64086408u, 0x64076407u);
 }
 
-// The same pair without its bias: q for even e, 16 q for odd e (an exact fp16
-// subtraction of 1032 = 0x6408 or 1152 = 0x6480).
+// The same pair as fp16 subnormals: (q + 8) * 2^-24 for even e, 16 (q + 8) *
+// 2^-24 for odd e (the nibble with its sign bit flipped is the significand;
+// one LOP3, no exponent bits).
+__device__ __forceinline__ uint32_t q4_pair_sub(uint32_t w, int e)
+{
+    const uint32_t x = (e & 2) ? (w >> 8) : w;
+    return (e & 1) ? lop3_ac(x, 0x00800080u, 0x00700070u) : lop3_ac(x, 0x00080008u, 0x00070007u);
+}
+
+// The pair without any offset: q for even e, 16 q for odd e (an exact fp16
+// subtraction of 1032 = 0x6408 or 1152 = 0x6480 from the biased form).
 __device__ __forceinline__ uint32_t q4_pair(uint32_t w, int e)
 {
     const uint32_t b = q4_pair_biased(w, e);
@@ -326,6 +339,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     // chunks cw and cw1 (= cw when it has at most two tiles).
     const int cw = (warp * MTW) >> 1, cw1 = (MTW == 4) ? cw + 1 : cw;
     constexpr int NGW = (MTW == 4 && VC == KVQ_CODEC_Q4_G32) ? 2 : 1;   // V groups a warp's tiles touch
+    constexpr bool kSubV = (NT == 1 && NGW == 1);                        // V codes as fp16 subnormals
     const int gv0 = (32 * cw) / group_size(VC);                          // the first of them
     const uint32_t voff0 =
         VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), ((lane >> 3) & 1) ? cw1 : cw);
@@ -533,6 +547,16 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         float msub[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) msub[nt] = (mg[nt] == -INFINITY) ? 0.0f : mg[nt];
+        // sum over the tile's tokens of P' per row (the same in all 16 accumulator
+        // rows), one per V group the warp touches, for removing the codes' offset
+        // (subnormal form only)
+        float psum[NGW][NT][4];
+#pragma unroll
+        for (int q = 0; q < NGW; ++q)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) psum[q][nt][c] = 0.0f;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
             // tokens past the split end have score -inf (p = 0) and V scale 0
@@ -568,11 +592,36 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 const int j = (MTW >= 2) ? (t & 1) : (warp & 1);
                 const int q = (NGW == 2) ? lc : 0;
                 const uint32_t ra = lc ? r1 : r0, rb = lc ? r3 : r2;
-                const uint32_t a0 = q4_pair(ra, 2 * j), a1 = q4_pair(ra, 2 * j + 1);
-                const uint32_t a2 = q4_pair(rb, 2 * j), a3 = q4_pair(rb, 2 * j + 1);
+                uint32_t a0, a1, a2, a3;
+                if constexpr (kSubV) {
+                    a0 = q4_pair_sub(ra, 2 * j); a1 = q4_pair_sub(ra, 2 * j + 1);
+                    a2 = q4_pair_sub(rb, 2 * j); a3 = q4_pair_sub(rb, 2 * j + 1);
+                } else {
+                    a0 = q4_pair(ra, 2 * j); a1 = q4_pair(ra, 2 * j + 1);
+                    a2 = q4_pair(rb, 2 * j); a3 = q4_pair(rb, 2 * j + 1);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[q][nt], b1[q][nt]);
             }
+            if constexpr (kSubV) {
+                constexpr uint32_t kOnes = 0x3C003C00u;             // fp16x2 (1, 1)
+#pragma unroll
+                for (int q = 0; q < NGW; ++q)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816(psum[q][nt], kOnes, kOnes, kOnes, kOnes, b0[q][nt], b1[q][nt]);
+            }
+        }
+        // remove the offset: 8 * 2^-24 per P' on rows 0-7 (even head_dim index),
+        // 128 * 2^-24 on rows 8-15 (odd index)
+#pragma unroll
+        for (int t = 0; kSubV && t < MTW; ++t) {
+            const int q = (NGW == 2) ? (t >> 1) : 0;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    o[t][nt][c] = fmaf(c < 2 ? -0x1p-21f : -0x1p-17f, psum[q][nt][c], o[t][nt][c]);
         }
     };
 
@@ -653,8 +702,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             const int n = nt * 8 + 2 * tig + cl;
             if (n >= R) continue;
             const bool empty = (M == -INFINITY || L <= 0.0f);
-            const float inv = empty ? 0.0f : 1.0f / L;
-            // rows of odd head_dim index were accumulated 16x (their codes' 1152 + 16 q form)
+            // the V codes entered as q 2^-24 or q (even head_dim index) and 16 times
+            // that (odd)
+            const float inv = empty ? 0.0f : (kSubV ? 0x1p24f : 1.0f) / L;
             const float inv16 = inv * 0.0625f;
             const int i = n / G, jj = n % G;
             const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
