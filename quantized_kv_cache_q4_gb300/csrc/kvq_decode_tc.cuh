@@ -1,8 +1,9 @@
 // kvq_decode_tc.cuh -- split-K decode / MTP-verify attention over a packed cache
 // on the tensor cores, for 1..32 query rows per kv head (GQA group x query
-// tokens), head_dim 64/128/256, K in Q4_G64, Q4_G32 or q8_0 and V in Q4_G64
-// or Q4_G32 (the kernel template; kvq_decode_tc.cu and kvq_decode_tc_g32.cu
-// hold its instances for the two V codecs, so that they compile in parallel)
+// tokens), head_dim 64/128/256, K and V each in Q4_G64, Q4_G32 or q8_0 (the
+// kernel template; kvq_decode_tc.cu, kvq_decode_tc_g32.cu and
+// kvq_decode_tc_q8v.cu hold its instances for the three V codecs, so that
+// they compile in parallel)
 // (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
 // this fork is": signed INT4 + one FP16 scale per 64 values; "Results": MTP
 // n-max 2, i.e. 1 + 2 query tokens per sequence).
@@ -51,7 +52,6 @@ namespace kvq {
 using namespace ptx;
 namespace {
 
-constexpr int kS = 3;                        // ring stages
 constexpr int kW = 4;                        // warps
 constexpr int kT = kW * 32;                  // threads
 
@@ -59,7 +59,7 @@ __device__ __forceinline__ void warps_sync() { asm volatile("bar.sync 1, %0;" ::
 
 template <int KC, int VC, int D, int NT, typename QT>
 struct TcCfg {
-    static constexpr int KRB = row_bytes(KC, D), VRB = D / 2;
+    static constexpr int KRB = row_bytes(KC, D), VRB = row_bytes(VC, D);
     static constexpr int KSB = 2 * scales_per_row(KC, D), VSB = 2 * scales_per_row(VC, D);
     static constexpr int NGK = D / group_size(KC);
     static constexpr int ROWS = NT * 8;                           // query rows kept (zero past R)
@@ -69,7 +69,10 @@ struct TcCfg {
     static constexpr int KS_OFF = V_OFF + align_up(kTile * VRB, 1024);
     static constexpr int VS_OFF = KS_OFF + align_up(kTile * KSB, 128);
     static constexpr int STAGE = align_up(VS_OFF + kTile * VSB, 1024);
-    static constexpr int QP_OFF = kS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
+    // ring stages: 3, or 2 where 3 would leave room for one CTA per SM only
+    // (q8_0 K and V: 34 KB a stage)
+    static constexpr int NS = STAGE <= 27 * 1024 ? 3 : 2;
+    static constexpr int QP_OFF = NS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
     static constexpr int KB_OFF = QP_OFF + ROWS * D * 2;          // fp32 [NGK][ROWS]: minus the K bias terms
     // the query rows as given are only read before the first tile, the score
     // tiles and the maxima only after it: they share one region
@@ -83,7 +86,7 @@ struct TcCfg {
     static constexpr int QST_BYTES = ROWS * D * (int)sizeof(QT);
     static constexpr int PR_BYTES = (VT_OFF - U_OFF) + 2 * NGV * kTile * 2;
     static constexpr int BAR_OFF = align_up(U_OFF + (QST_BYTES > PR_BYTES ? QST_BYTES : PR_BYTES), 16);
-    static constexpr int SMEM = BAR_OFF + (kS + 1) * 8 + 1024;            // + alignment slack
+    static constexpr int SMEM = BAR_OFF + (NS + 1) * 8 + 1024;            // + alignment slack
     static constexpr int MTW = (D / 64 * 4) / kW;                 // 16-row head_dim tiles per warp in phase B
     // CTAs per SM the kernel is built for (shared memory allows 3 up to 16 rows)
     static constexpr int MIN_BLOCKS = NT <= 2 ? 3 : 2;
@@ -141,6 +144,30 @@ __device__ __forceinline__ uint32_t q4_pair_sub(uint32_t w, int e)
 {
     const uint32_t x = (e & 2) ? (w >> 8) : w;
     return (e & 1) ? lop3_ac(x, 0x00800080u, 0x00700070u) : lop3_ac(x, 0x00080008u, 0x00070007u);
+}
+
+// q8_0 V after ldmatrix.trans: a word holds head_dim bytes (d, d + 1) of two
+// tokens, [t0 d, t0 d+1, t1 d, t1 d+1]; the A fragment wants (t0, t1) at one d.
+// As fp16 subnormals (q + 128) 2^-24: even d = (w ^ 0x80 per byte) & 0x00FF00FF
+// (one LOP3, 0x28 = (a ^ b) & c), odd d the same on bytes 1, 3 moved down.
+__device__ __forceinline__ void q8_pairs_sub(uint32_t w, uint32_t &ev, uint32_t &od)
+{
+    uint32_t hi;
+    asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(ev) : "r"(w), "r"(0x00800080u), "r"(0x00FF00FFu));
+    asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(hi) : "r"(w), "r"(0x80008000u), "r"(0xFF00FF00u));
+    od = hi >> 8;
+}
+
+// The same pairs without offset: q exactly (1152 + q from the exponent byte
+// 0x64, then an exact fp16 subtraction of 1152 = 0x6480).
+__device__ __forceinline__ void q8_pairs(uint32_t w, uint32_t &ev, uint32_t &od)
+{
+    const uint32_t x = w ^ 0x80808080u;
+    uint32_t e, o;
+    asm("prmt.b32 %0, %1, %2, 0x4240;" : "=r"(e) : "r"(x), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4341;" : "=r"(o) : "r"(x), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(ev) : "r"(e), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(od) : "r"(o), "r"(0x64806480u));
 }
 
 // The pair without any offset: q for even e, 16 q for odd e (an exact fp16
@@ -223,6 +250,7 @@ __global__ void __launch_bounds__(kT, (TcCfg<KC, VC, D, NT, QT>::MIN_BLOCKS))
 decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
 {
     using C = TcCfg<KC, VC, D, NT, QT>;
+    constexpr int kS = C::NS;
     using KG = TileGeom<C::KRB>;
     using VG = TileGeom<C::VRB>;
     constexpr int NGK = C::NGK;
@@ -337,12 +365,22 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     // pair 2 (mt % 2) (even head_dim index), rows 8-15 the pair 2 (mt % 2) + 1
     // (odd index), so a tile never spans two V groups.  The warp's tiles lie in
     // chunks cw and cw1 (= cw when it has at most two tiles).
+    // q8_0 V instead: tile t is the 16-byte chunk MTW * warp + t (16 head_dim
+    // values), rows 0-7 its even, rows 8-15 its odd head_dim indices; one
+    // ldmatrix.x4.trans covers two chunks.
+    constexpr bool V8 = (VC == KVQ_CODEC_Q8_0);
     const int cw = (warp * MTW) >> 1, cw1 = (MTW == 4) ? cw + 1 : cw;
-    constexpr int NGW = (MTW == 4 && VC == KVQ_CODEC_Q4_G32) ? 2 : 1;   // V groups a warp's tiles touch
-    constexpr bool kSubV = (NT == 1 && NGW == 1);                        // V codes as fp16 subnormals
-    const int gv0 = (32 * cw) / group_size(VC);                          // the first of them
-    const uint32_t voff0 =
-        VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), ((lane >> 3) & 1) ? cw1 : cw);
+    constexpr int NGW = (MTW == 4 && VC != KVQ_CODEC_Q4_G64) ? 2 : 1;    // V groups a warp's tiles touch
+    // V codes as fp16 subnormals with their offset removed per tile (one n-tile)
+    constexpr bool kSubV = (NT == 1 && (NGW == 1 || V8));
+    const int gv0 = V8 ? (MTW * warp) / 2 : (32 * cw) / group_size(VC);  // the first of them
+    constexpr int NLV = V8 ? (MTW + 1) / 2 : 1;                          // ldmatrix per 16 tokens
+    uint32_t voff[NLV];
+#pragma unroll
+    for (int u = 0; u < NLV; ++u) {
+        const int ca = V8 ? MTW * warp + 2 * u : cw, cb = V8 ? (MTW >= 2 ? ca + 1 : ca) : cw1;
+        voff[u] = VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), ((lane >> 3) & 1) ? cb : ca);
+    }
     const uint32_t qp_base = smem_u32(qp);
     // with one n-tile the query's B fragments fit in registers for the whole CTA
     constexpr bool QREG = (NT == 1);
@@ -560,8 +598,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
             // tokens past the split end have score -inf (p = 0) and V scale 0
-            uint32_t r0, r1, r2, r3;           // tokens 0-7 / 8-15 of chunks cw and cw1
-            ldsm_x4_t(base + voff0 + (uint32_t)(16 * kk * VG::BI), r0, r1, r2, r3);
+            // tokens 0-7 of chunks a, b, tokens 8-15 of chunks a, b
+            uint32_t rv[NLV][4];
+#pragma unroll
+            for (int u = 0; u < NLV; ++u)
+                ldsm_x4_t(base + voff[u] + (uint32_t)(16 * kk * VG::BI), rv[u][0], rv[u][1], rv[u][2], rv[u][3]);
             float p[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -587,12 +628,28 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             }
 #pragma unroll
             for (int t = 0; t < MTW; ++t) {
+                const int q = (NGW == 2) ? (t >> 1) : 0;
+                uint32_t a0, a1, a2, a3;
+                if constexpr (V8) {
+                    // tile t: load t / 2, chunk a or b by t's parity
+                    const int u = t >> 1;
+                    const bool b = (MTW >= 2) && (t & 1);
+                    const uint32_t ra = b ? rv[u][1] : rv[u][0], rb = b ? rv[u][3] : rv[u][2];
+                    if constexpr (kSubV) {
+                        q8_pairs_sub(ra, a0, a1);
+                        q8_pairs_sub(rb, a2, a3);
+                    } else {
+                        q8_pairs(ra, a0, a1);
+                        q8_pairs(rb, a2, a3);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816(o[t][nt], a0, a1, a2, a3, b0[q][nt], b1[q][nt]);
+                    continue;
+                }
                 // tile t: chunk cw + lc, nibble pairs 2j (rows 0-7) and 2j + 1 (rows 8-15)
                 const int lc = (MTW >= 2) ? (t >> 1) : 0;
                 const int j = (MTW >= 2) ? (t & 1) : (warp & 1);
-                const int q = (NGW == 2) ? lc : 0;
-                const uint32_t ra = lc ? r1 : r0, rb = lc ? r3 : r2;
-                uint32_t a0, a1, a2, a3;
+                const uint32_t ra = lc ? rv[0][1] : rv[0][0], rb = lc ? rv[0][3] : rv[0][2];
                 if constexpr (kSubV) {
                     a0 = q4_pair_sub(ra, 2 * j); a1 = q4_pair_sub(ra, 2 * j + 1);
                     a2 = q4_pair_sub(rb, 2 * j); a3 = q4_pair_sub(rb, 2 * j + 1);
@@ -612,8 +669,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                         mma16816(psum[q][nt], kOnes, kOnes, kOnes, kOnes, b0[q][nt], b1[q][nt]);
             }
         }
-        // remove the offset: 8 * 2^-24 per P' on rows 0-7 (even head_dim index),
-        // 128 * 2^-24 on rows 8-15 (odd index)
+        // remove the offset: Q4 8 * 2^-24 per P' on rows 0-7 (even head_dim
+        // index), 128 * 2^-24 on rows 8-15 (odd index); q8_0 128 * 2^-24
 #pragma unroll
         for (int t = 0; kSubV && t < MTW; ++t) {
             const int q = (NGW == 2) ? (t >> 1) : 0;
@@ -621,7 +678,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    o[t][nt][c] = fmaf(c < 2 ? -0x1p-21f : -0x1p-17f, psum[q][nt][c], o[t][nt][c]);
+                    o[t][nt][c] = fmaf((c < 2 && !V8) ? -0x1p-21f : -0x1p-17f, psum[q][nt][c], o[t][nt][c]);
         }
     };
 
@@ -702,14 +759,20 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             const int n = nt * 8 + 2 * tig + cl;
             if (n >= R) continue;
             const bool empty = (M == -INFINITY || L <= 0.0f);
-            // the V codes entered as q 2^-24 or q (even head_dim index) and 16 times
-            // that (odd)
+            // the V codes entered as q 2^-24 or q (even head_dim index) and, for the
+            // 4-bit codecs, 16 times that (odd)
             const float inv = empty ? 0.0f : (kSubV ? 0x1p24f : 1.0f) / L;
-            const float inv16 = inv * 0.0625f;
+            const float inv16 = V8 ? inv : inv * 0.0625f;
             const int i = n / G, jj = n % G;
             const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
             float *dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
-            if constexpr (MTW >= 2) {
+            if constexpr (V8) {
+                // tile t: head_dim 16 (MTW warp + t) + 2 gid (+ 1)
+#pragma unroll
+                for (int t = 0; t < MTW; ++t)
+                    *reinterpret_cast<float2 *>(dst + 16 * (MTW * warp + t) + 2 * gid) =
+                        make_float2(o[t][nt][cl] * inv, o[t][nt][cl + 2] * inv16);
+            } else if constexpr (MTW >= 2) {
                 // tiles 2 lc and 2 lc + 1 fill head_dim 32 (cw + lc) + 4 gid + 0..3
 #pragma unroll
                 for (int lc = 0; lc < MTW / 2; ++lc)

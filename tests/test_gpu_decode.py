@@ -74,11 +74,11 @@ def test_codec_pairs(kc, vc, D):
 
 
 @pytest.mark.parametrize("kc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32])
-@pytest.mark.parametrize("vc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G32])
+@pytest.mark.parametrize("vc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0])
 @pytest.mark.parametrize("G,n_new", [(1, 1), (6, 3), (8, 4)])
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
-    """Every K codec with both 4-bit V codecs, at 1..32 query rows per kv head
+    """Every K codec with every V codec, at 1..32 query rows per kv head
     (one to four 8-row n-tiles) and a ragged last tile."""
     wl = workloads.custom(n_seq=2, n_heads=2 * G, n_kv_heads=2, head_dim=D, cached=(900 - n_new, 161), n_new=n_new,
                           k_codec=kc, v_codec=vc, src_dtype="f16", q_dtype="f16", dist="outliers",
@@ -86,6 +86,22 @@ def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
     k, v, ko, vo = _both(wl)
     o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
     for n_splits in (0, 3):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0),
+                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32)])
+@pytest.mark.parametrize("D", [128, 256])
+def test_more_than_32_rows_per_kv_head(kc, vc, D):
+    """12 query heads per kv head x 3 query tokens = 36 rows: past the
+    tensor-core kernel's 32, the SIMT kernel runs."""
+    wl = workloads.custom(n_seq=2, n_heads=12, n_kv_heads=1, head_dim=D, cached=(600, 77), n_new=3, k_codec=kc,
+                          v_codec=vc, src_dtype="f16", q_dtype="f16", seed=5 * kc + vc + D)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (0, 2):
         o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
         assert err == 0
         check_close(o, o_ref, lse, lse_ref)
