@@ -5,13 +5,13 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 library never calls it, and it shares no code with the CUDA library: the C
 source next to this file states the codec and the attention from their
 definitions (den_llama.cpp, "What this fork is" and the "build3 (working
-engine) -- additions" table for Q4_G64; the mixed "-ctk q8_0 -ctv q4_g64"
-pair of the "Build3 (working engine)" command block).
+engine) -- additions" table for Q4_G64 and the NVFP4 KV type; the mixed
+"-ctk q8_0 -ctv q4_g64" pair of the "Build3 (working engine)" command block).
 
 Every function takes and returns numpy arrays.  Parity status: every function
 here is pinned by ``tests/test_oracle_*.py`` (closed forms, a hand-worked
-golden block, numpy's float16 conversion, torch's float64 attention, exact
-rational brute force, invariants).
+golden block, numpy's float16 and torch's float8_e4m3fn conversions, torch's
+float64 attention, exact rational brute force, invariants).
 """
 from __future__ import annotations
 
@@ -26,8 +26,11 @@ import numpy as np
 Q4_G64 = 1
 Q8_0 = 2
 Q4_G32 = 3                  # the pages' "q4_0", read as Q4_G64 with 32-value groups
-GROUP = {Q4_G64: 64, Q8_0: 32, Q4_G32: 32}
-FOUR_BIT = (Q4_G64, Q4_G32)
+NVFP4 = 4                   # E2M1 values, one E4M3 scale per 16 (NVIDIA's NVFP4, no tensor scale)
+GROUP = {Q4_G64: 64, Q8_0: 32, Q4_G32: 32, NVFP4: 16}
+FOUR_BIT = (Q4_G64, Q4_G32)                 # integer 4-bit codes
+NIBBLE = (Q4_G64, Q4_G32, NVFP4)            # two codes per byte
+SCALE_DTYPE = {Q4_G64: np.uint16, Q8_0: np.uint16, Q4_G32: np.uint16, NVFP4: np.uint8}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
@@ -56,6 +59,12 @@ def _declare(lib):
     lib.orc_f16_to_f32.restype = ctypes.c_float
     lib.orc_f32_to_f16_array.argtypes = [P, I64, P]
     lib.orc_f16_to_f32_array.argtypes = [P, I64, P]
+    lib.orc_f32_to_e4m3_array.argtypes = [P, I64, P]
+    lib.orc_f32_to_e2m1_array.argtypes = [P, I64, P]
+    lib.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_to_f32.restype = ctypes.c_float
+    lib.orc_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_to_f32.restype = ctypes.c_float
     lib.orc_quantize.argtypes = [I, P, I64, I, P, P]
     lib.orc_dequantize.argtypes = [I, P, P, I64, I, P]
     lib.orc_quantize_append.argtypes = [I, P, I, I, I, I, I, P, P, P]
@@ -109,7 +118,7 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def row_bytes(codec: int, head_dim: int) -> int:
-    return head_dim // 2 if codec in FOUR_BIT else head_dim
+    return head_dim // 2 if codec in NIBBLE else head_dim
 
 
 def scales_per_row(codec: int, head_dim: int) -> int:
@@ -133,6 +142,34 @@ def f16_bits_to_f32(h) -> np.ndarray:
     return out
 
 
+def f32_to_e4m3(x) -> np.ndarray:
+    """fp32 -> E4M3 bytes, round to nearest even, saturating at 448."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib.orc_f32_to_e4m3_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def f32_to_e2m1(x) -> np.ndarray:
+    """fp32 -> E2M1 codes (low nibble), round to nearest even, saturating at 6."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib.orc_f32_to_e2m1_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e4m3_to_f32(b) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.orc_e4m3_to_f32(int(v)) for v in np.ravel(b)], np.float32).reshape(np.shape(b))
+
+
+def e2m1_to_f32(n) -> np.ndarray:
+    lib = _load()
+    return np.array([lib.orc_e2m1_to_f32(int(v)) for v in np.ravel(n)], np.float32).reshape(np.shape(n))
+
+
 def _as_f32_rows(x: np.ndarray) -> np.ndarray:
     """Widen fp16/fp32 inputs to fp32 (exact)."""
     if x.dtype == np.float16:
@@ -141,13 +178,14 @@ def _as_f32_rows(x: np.ndarray) -> np.ndarray:
 
 
 def quantize(codec: int, x: np.ndarray):
-    """Quantize rows x[..., head_dim] -> (qs uint8 [..., row_bytes], scales uint16 fp16 bits)."""
+    """Quantize rows x[..., head_dim] -> (qs uint8 [..., row_bytes], scales: fp16 bit
+    patterns as uint16, or E4M3 bytes as uint8 for NVFP4)."""
     lib = _load()
     x = _as_f32_rows(x)
     D = x.shape[-1]
     n = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
     qs = np.zeros(x.shape[:-1] + (row_bytes(codec, D),), dtype=np.uint8)
-    sc = np.zeros(x.shape[:-1] + (scales_per_row(codec, D),), dtype=np.uint16)
+    sc = np.zeros(x.shape[:-1] + (scales_per_row(codec, D),), dtype=SCALE_DTYPE[codec])
     lib.orc_quantize(codec, _ptr(x), n, D, _ptr(qs), _ptr(sc))
     return qs, sc
 
@@ -155,7 +193,7 @@ def quantize(codec: int, x: np.ndarray):
 def dequantize(codec: int, qs: np.ndarray, sc: np.ndarray, head_dim: int) -> np.ndarray:
     lib = _load()
     qs = np.ascontiguousarray(qs, dtype=np.uint8)
-    sc = np.ascontiguousarray(sc, dtype=np.uint16)
+    sc = np.ascontiguousarray(sc, dtype=SCALE_DTYPE[codec])
     n = qs.size // row_bytes(codec, head_dim)
     out = np.empty(qs.shape[:-1] + (head_dim,), dtype=np.float32)
     lib.orc_dequantize(codec, _ptr(qs), _ptr(sc), n, head_dim, _ptr(out))
@@ -169,7 +207,7 @@ class Cache:
         self.codec, self.n_seq, self.n_kv_heads = codec, n_seq, n_kv_heads
         self.head_dim, self.capacity = head_dim, capacity
         self.qs = np.zeros((n_seq, n_kv_heads, capacity, row_bytes(codec, head_dim)), np.uint8)
-        self.scales = np.zeros((n_seq, n_kv_heads, capacity, scales_per_row(codec, head_dim)), np.uint16)
+        self.scales = np.zeros((n_seq, n_kv_heads, capacity, scales_per_row(codec, head_dim)), SCALE_DTYPE[codec])
 
 
 def quantize_append(cache: Cache, src: np.ndarray, pos0: np.ndarray) -> int:

@@ -20,6 +20,16 @@
  *     "Results": the 65K serve run) is not defined on the pages; it is read as
  *     the Q4_G64 rule and nibble layout with groups of 32 values (4.5 bits per
  *     value).
+ *   - NVFP4, the pages' KV type of the matched "-ctk nvfp4 -ctv nvfp4" and
+ *     mixed "-ctk q8_0 -ctv nvfp4" runs (den_llama.cpp, "What this fork is",
+ *     quantized KV cache bullet; "build3 (working engine) -- additions" table,
+ *     NVFP4 KV row; "Build3" command block), whose format the pages do not
+ *     give: read as NVIDIA's published NVFP4 -- FP4 E2M1 values in blocks of
+ *     16, each block with one FP8 E4M3 scale -- without the per-tensor second
+ *     scale (a cache is appended to row by row, so no tensor-wide absmax
+ *     exists when a row is written): scale = e4m3(absmax / 6), code =
+ *     e2m1(x / (float)scale), both round-to-nearest-even on their format's
+ *     grid and held at the largest finite value (448, 6); 4.5 bits per value.
  *   - The q8_0-style K codec of the mixed pair "-ctk q8_0 -ctv q4_g64"
  *     (den_llama.cpp, "Build3 (working engine)" command block): 32 int8 values
  *     with one FP16 scale, scale = fp16(absmax / 127), q = clamp(rne(x/scale),
@@ -48,6 +58,7 @@
 #define ORC_Q4 1
 #define ORC_Q8 2
 #define ORC_Q4_32 3
+#define ORC_NVFP4 4
 
 /* ------------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> binary32, written from the format definition.      */
@@ -111,22 +122,96 @@ void orc_f16_to_f32_array(const uint16_t *h, int64_t n, float *out)
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 E4M3 and FP4 E2M1, written from their format definitions.            */
+/* ------------------------------------------------------------------------ */
+
+/* E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0
+ * holds the subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448. */
+float orc_e4m3_to_f32(uint8_t b)
+{
+    int e = (b >> 3) & 15, m = b & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = (float)m * ldexpf(1.0f, -9);
+    else v = (1.0f + (float)m / 8.0f) * ldexpf(1.0f, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+/* E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent field 0
+ * holds the subnormal m * 0.5.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+float orc_e2m1_to_f32(uint8_t n)
+{
+    int e = (n >> 1) & 3, m = n & 1;
+    float v = (e == 0) ? 0.5f * (float)m : (1.0f + 0.5f * (float)m) * ldexpf(1.0f, e - 1);
+    return (n & 8) ? -v : v;
+}
+
+/* Nearest of the n_codes non-negative finite values of a small format to |f|:
+ * at or past the largest value, the largest (the saturation the formats are
+ * used with); otherwise the code whose value is closest (exact: every
+ * candidate and |f| are floats below the largest value, their differences
+ * are formed in double), ties to the even code (even mantissa). */
+static int orc_nearest_code(float a, int n_codes, float (*decode)(uint8_t))
+{
+    if (a >= decode((uint8_t)(n_codes - 1))) return n_codes - 1;
+    int best = 0;
+    double bd = fabs((double)a - (double)decode(0));
+    for (int c = 1; c < n_codes; ++c) {
+        double d = fabs((double)a - (double)decode((uint8_t)c));
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return best;
+}
+
+/* binary32 -> E4M3 / E2M1: round to nearest, ties to even, saturating; the
+ * sign bit is the input's (so a negative value that rounds to zero is -0).
+ * Finite inputs. */
+uint8_t orc_f32_to_e4m3(float f)
+{
+    int c = orc_nearest_code(fabsf(f), 127, orc_e4m3_to_f32);      /* 0x00 .. 0x7E */
+    return (uint8_t)(c | (signbit(f) ? 0x80 : 0));
+}
+
+uint8_t orc_f32_to_e2m1(float f)
+{
+    int c = orc_nearest_code(fabsf(f), 8, orc_e2m1_to_f32);
+    return (uint8_t)(c | (signbit(f) ? 8 : 0));
+}
+
+void orc_f32_to_e4m3_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e4m3(x[i]);
+}
+
+void orc_f32_to_e2m1_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_e2m1(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Codec                                                                    */
 /* ------------------------------------------------------------------------ */
 
-/* 4-bit codecs: Q4_G64 and Q4_G32 (the same rule and nibble layout with 32-value groups). */
+/* Integer 4-bit codecs: Q4_G64 and Q4_G32 (the same rule and nibble layout with 32-value groups). */
 static int orc_is4(int codec) { return codec == ORC_Q4 || codec == ORC_Q4_32; }
-static int orc_group(int codec) { return codec == ORC_Q4 ? 64 : 32; }
+static int orc_group(int codec) { return codec == ORC_Q4 ? 64 : codec == ORC_NVFP4 ? 16 : 32; }
 static int orc_qmax(int codec) { return orc_is4(codec) ? 7 : 127; }
 static int orc_qmin(int codec) { return orc_is4(codec) ? -8 : -127; }
 
 /* Bytes of the code plane per row of head_dim values. */
 int orc_row_bytes(int codec, int head_dim)
 {
-    return orc_is4(codec) ? head_dim / 2 : head_dim;
+    return (orc_is4(codec) || codec == ORC_NVFP4) ? head_dim / 2 : head_dim;
 }
 
 int orc_scales_per_row(int codec, int head_dim) { return head_dim / orc_group(codec); }
+
+/* Bytes of one scale: fp16 bit patterns, except NVFP4's E4M3 bytes. */
+int orc_scale_bytes(int codec) { return codec == ORC_NVFP4 ? 1 : 2; }
 
 /* Scale of one group: fp16(absmax / qmax), the fp32 quotient rounded once to
  * fp16; a result past the largest finite half is held at 65504. */
@@ -154,17 +239,49 @@ static int orc_code(float x, float d, int qmin, int qmax)
     return (int)r;
 }
 
+/* NVFP4 block: scale = e4m3(absmax / 6) with the fp32 quotient; codes
+ * e2m1(x / (float)scale), all 0 when the scale is 0.  Codes go to c[0..n). */
+static uint8_t orc_nvfp4_block(const float *x, int n, uint8_t *c)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    uint8_t sb = orc_f32_to_e4m3(amax / 6.0f);
+    float d = orc_e4m3_to_f32(sb);
+    for (int i = 0; i < n; ++i) c[i] = (d == 0.0f) ? 0 : orc_f32_to_e2m1(x[i] / d);
+    return sb;
+}
+
 /* Quantize n_rows rows of head_dim fp32 values.
  * Q4_G64: qs row = head_dim/2 bytes; byte j holds value 2j in its low nibble
  *         and value 2j+1 in its high nibble, each as a 4-bit two's complement
  *         code; scales row = head_dim/64 fp16 bit patterns, group order.
  * Q4_G32: the same with groups of 32 values (head_dim/32 scales).
- * Q8_0:   qs row = head_dim int8 codes; scales row = head_dim/32 fp16. */
+ * Q8_0:   qs row = head_dim int8 codes; scales row = head_dim/32 fp16.
+ * NVFP4:  qs row as Q4_G64 with E2M1 codes; scales row = head_dim/16 E4M3
+ *         bytes (scales is a byte array for this codec). */
 void orc_quantize(int codec, const float *x, int64_t n_rows, int head_dim,
-                  uint8_t *qs, uint16_t *scales)
+                  uint8_t *qs, void *scales)
 {
-    int gs = orc_group(codec), qmax = orc_qmax(codec), qmin = orc_qmin(codec);
-    int rb = orc_row_bytes(codec, head_dim), ng = head_dim / gs;
+    int gs = orc_group(codec), rb = orc_row_bytes(codec, head_dim), ng = head_dim / gs;
+    if (codec == ORC_NVFP4) {
+        uint8_t *sc = (uint8_t *)scales, c[16];
+        for (int64_t r = 0; r < n_rows; ++r)
+            for (int g = 0; g < ng; ++g) {
+                sc[r * ng + g] = orc_nvfp4_block(x + r * head_dim + g * gs, gs, c);
+                for (int i = 0; i < gs; ++i) {
+                    int v = g * gs + i;
+                    uint8_t *b = qs + r * rb + (v >> 1);
+                    if (v & 1) *b = (uint8_t)((*b & 0x0F) | (c[i] << 4));
+                    else       *b = (uint8_t)((*b & 0xF0) | c[i]);
+                }
+            }
+        return;
+    }
+    uint16_t *sc16 = (uint16_t *)scales;
+    int qmax = orc_qmax(codec), qmin = orc_qmin(codec);
     for (int64_t r = 0; r < n_rows; ++r) {
         const float *xr = x + r * head_dim;
         uint8_t *qr = qs + r * rb;
@@ -172,7 +289,7 @@ void orc_quantize(int codec, const float *x, int64_t n_rows, int head_dim,
             const float *xg = xr + g * gs;
             uint16_t dh = orc_group_scale(xg, gs, qmax);
             float d = orc_f16_to_f32(dh);
-            scales[r * ng + g] = dh;
+            sc16[r * ng + g] = dh;
             for (int i = 0; i < gs; ++i) {
                 int q = orc_code(xg[i], d, qmin, qmax);
                 int v = g * gs + i;
@@ -198,15 +315,23 @@ static int orc_get_code(int codec, const uint8_t *qr, int v)
     return (int)(int8_t)qr[v];
 }
 
-/* Dequantize rows: x_hat = (float)scale * (float)code, exact in fp32. */
-void orc_dequantize(int codec, const uint8_t *qs, const uint16_t *scales,
+/* Dequantize rows: x_hat = (float)scale * (float)code, exact in fp32 (NVFP4:
+ * e4m3 scale times e2m1 value, 4 x 2 significant bits). */
+void orc_dequantize(int codec, const uint8_t *qs, const void *scales,
                     int64_t n_rows, int head_dim, float *out)
 {
     int gs = orc_group(codec), rb = orc_row_bytes(codec, head_dim), ng = head_dim / gs;
     for (int64_t r = 0; r < n_rows; ++r) {
         for (int v = 0; v < head_dim; ++v) {
-            float d = orc_f16_to_f32(scales[r * ng + v / gs]);
-            out[r * head_dim + v] = d * (float)orc_get_code(codec, qs + r * rb, v);
+            const uint8_t *qr = qs + r * rb;
+            if (codec == ORC_NVFP4) {
+                float d = orc_e4m3_to_f32(((const uint8_t *)scales)[r * ng + v / gs]);
+                uint8_t nib = (v & 1) ? (qr[v >> 1] >> 4) : (qr[v >> 1] & 0xF);
+                out[r * head_dim + v] = d * orc_e2m1_to_f32(nib);
+            } else {
+                float d = orc_f16_to_f32(((const uint16_t *)scales)[r * ng + v / gs]);
+                out[r * head_dim + v] = d * (float)orc_get_code(codec, qr, v);
+            }
         }
     }
 }
@@ -217,17 +342,18 @@ void orc_dequantize(int codec, const uint8_t *qs, const uint16_t *scales,
  * fall outside [0, capacity) is skipped and bit 0 of the return value set. */
 int orc_quantize_append(int codec, const float *src, int n_seq, int n_new, int n_kv_heads,
                         int head_dim, int capacity, const int32_t *pos0,
-                        uint8_t *qs, uint16_t *scales)
+                        uint8_t *qs, void *scales)
 {
     int err = 0;
-    int rb = orc_row_bytes(codec, head_dim), ng = orc_scales_per_row(codec, head_dim);
+    int rb = orc_row_bytes(codec, head_dim);
+    int64_t sb = (int64_t)orc_scales_per_row(codec, head_dim) * orc_scale_bytes(codec);
     for (int s = 0; s < n_seq; ++s) {
         if (pos0[s] < 0 || (int64_t)pos0[s] + n_new > capacity) { err |= 1; continue; }
         for (int i = 0; i < n_new; ++i)
             for (int h = 0; h < n_kv_heads; ++h) {
                 const float *x = src + (((int64_t)s * n_new + i) * n_kv_heads + h) * head_dim;
                 int64_t row = ((int64_t)s * n_kv_heads + h) * capacity + pos0[s] + i;
-                orc_quantize(codec, x, 1, head_dim, qs + row * rb, scales + row * ng);
+                orc_quantize(codec, x, 1, head_dim, qs + row * rb, (uint8_t *)scales + row * sb);
             }
     }
     return err;
@@ -249,7 +375,7 @@ static int64_t orc_visible(int32_t kv_len, int n_q, int i)
 typedef struct {
     int k_codec, v_codec;
     const uint8_t *k_qs, *v_qs;
-    const uint16_t *k_sc, *v_sc;
+    const uint8_t *k_sc, *v_sc;     /* scale planes as bytes (fp16 or E4M3 elements) */
     int n_seq, n_kv_heads, head_dim, capacity;
     const float *q;            /* [n_seq][n_q][n_heads][head_dim] */
     int n_q, n_heads;
@@ -275,7 +401,8 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     double *qd = (double *)malloc(sizeof(double) * (size_t)(R * D));
     int64_t *nv = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
     int krb = orc_row_bytes(a->k_codec, D), vrb = orc_row_bytes(a->v_codec, D);
-    int kng = orc_scales_per_row(a->k_codec, D), vng = orc_scales_per_row(a->v_codec, D);
+    int64_t ksb = (int64_t)orc_scales_per_row(a->k_codec, D) * orc_scale_bytes(a->k_codec);
+    int64_t vsb = (int64_t)orc_scales_per_row(a->v_codec, D) * orc_scale_bytes(a->v_codec);
 
     /* row r = i * G + j is query token i, query head kh * G + j */
     for (int i = 0; i < a->n_q; ++i)
@@ -292,7 +419,7 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     /* pass 1: scores */
     for (int64_t t = 0; t < span; ++t) {
         int64_t row = plane + t_lo + t;
-        orc_dequantize(a->k_codec, a->k_qs + row * krb, a->k_sc + row * kng, 1, D, kr);
+        orc_dequantize(a->k_codec, a->k_qs + row * krb, a->k_sc + row * ksb, 1, D, kr);
         for (int r = 0; r < R; ++r) {
             if (t >= nv[r]) continue;
             double acc = 0.0;
@@ -319,7 +446,7 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
         int need = 0;
         for (int r = 0; r < R; ++r) need |= (t < nv[r]);
         if (!need) continue;
-        orc_dequantize(a->v_codec, a->v_qs + row * vrb, a->v_sc + row * vng, 1, D, vr);
+        orc_dequantize(a->v_codec, a->v_qs + row * vrb, a->v_sc + row * vsb, 1, D, vr);
         for (int r = 0; r < R; ++r) {
             if (t >= nv[r]) continue;
             double p = z[r * span + t];
@@ -360,13 +487,13 @@ static void orc_attend_unit_to_output(const orc_attn_args *a, int s, int kh, int
  * out_lse [n_seq][n_q][n_heads] fp64 (natural log).  q is fp32 (the fp16 or
  * fp32 inputs widened exactly).  n_threads > 1 spreads (seq, kv head) units
  * over OpenMP threads; the arithmetic per unit is unchanged. */
-void orc_decode_attention(int k_codec, const uint8_t *k_qs, const uint16_t *k_sc,
-                          int v_codec, const uint8_t *v_qs, const uint16_t *v_sc,
+void orc_decode_attention(int k_codec, const uint8_t *k_qs, const void *k_sc,
+                          int v_codec, const uint8_t *v_qs, const void *v_sc,
                           int n_seq, int n_kv_heads, int head_dim, int capacity,
                           const float *q, int n_q, int n_heads, const int32_t *kv_len,
                           double scale, double *out, double *out_lse, int n_threads)
 {
-    orc_attn_args a = {k_codec, v_codec, k_qs, v_qs, k_sc, v_sc, n_seq, n_kv_heads, head_dim,
+    orc_attn_args a = {k_codec, v_codec, k_qs, v_qs, (const uint8_t *)k_sc, (const uint8_t *)v_sc, n_seq, n_kv_heads, head_dim,
                        capacity, q, n_q, n_heads, kv_len, scale};
     int units = n_seq * n_kv_heads;
 #ifdef _OPENMP
@@ -386,13 +513,13 @@ void orc_decode_attention(int k_codec, const uint8_t *k_qs, const uint16_t *k_sc
  * of each chunk.  part_o is [n_splits][n_seq][n_q][n_heads][head_dim],
  * part_lse [n_splits][n_seq][n_q][n_heads]; an empty part has o = 0 and
  * lse = -inf. */
-void orc_decode_attention_split(int k_codec, const uint8_t *k_qs, const uint16_t *k_sc,
-                                int v_codec, const uint8_t *v_qs, const uint16_t *v_sc,
+void orc_decode_attention_split(int k_codec, const uint8_t *k_qs, const void *k_sc,
+                                int v_codec, const uint8_t *v_qs, const void *v_sc,
                                 int n_seq, int n_kv_heads, int head_dim, int capacity,
                                 const float *q, int n_q, int n_heads, const int32_t *kv_len,
                                 double scale, int n_splits, double *part_o, double *part_lse)
 {
-    orc_attn_args a = {k_codec, v_codec, k_qs, v_qs, k_sc, v_sc, n_seq, n_kv_heads, head_dim,
+    orc_attn_args a = {k_codec, v_codec, k_qs, v_qs, (const uint8_t *)k_sc, (const uint8_t *)v_sc, n_seq, n_kv_heads, head_dim,
                        capacity, q, n_q, n_heads, kv_len, scale};
     int64_t rows = (int64_t)n_seq * n_q * n_heads;
     for (int sp = 0; sp < n_splits; ++sp)

@@ -49,7 +49,8 @@ def _torch_reference(wl, kc, vc):
 
 
 @pytest.mark.parametrize("kc,vc", [(workloads.Q4_G64, workloads.Q4_G64), (workloads.Q8_0, workloads.Q4_G64),
-                                   (workloads.Q8_0, workloads.Q4_G32)])
+                                   (workloads.Q8_0, workloads.Q4_G32), (workloads.NVFP4, workloads.NVFP4),
+                                   (workloads.Q8_0, workloads.NVFP4)])
 @pytest.mark.parametrize("n_new", [1, 2, 3])
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_matches_torch_sdpa_float64(kc, vc, n_new, D):

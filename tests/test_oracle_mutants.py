@@ -8,8 +8,9 @@ import oracle
 import test_oracle_attention as ta
 import test_oracle_codec as tc
 import test_oracle_fp16 as tf
+import test_oracle_nvfp4 as tn
 
-Q4, Q8, Q4_32 = oracle.Q4_G64, oracle.Q8_0, oracle.Q4_G32
+Q4, Q8, Q4_32, NV = oracle.Q4_G64, oracle.Q8_0, oracle.Q4_G32, oracle.NVFP4
 
 PINS = [
     ("golden q4", lambda: tc.test_golden_rows("q4g64_two_groups.txt", Q4)),
@@ -26,7 +27,17 @@ PINS = [
     ("split/merge", lambda: ta.test_split_then_merge_equals_unsplit(3)),
     ("merge closed forms", ta.test_merge_closed_forms),
     ("fraction brute force", lambda: ta.test_exact_rational_brute_force(5)),
+    ("golden nvfp4", tn.test_golden_row),
+    ("e2m1 binade", tn.test_e2m1_encode_matches_binade_rounding),
+    ("e2m1 ties", tn.test_e2m1_ties_and_signed_zero),
+    ("e4m3 binade", tn.test_e4m3_encode_matches_binade_rounding_and_saturates),
+    ("nvfp4 rule", lambda: tn.test_quantize_matches_the_rule_written_another_way("mixed")),
+    ("nvfp4 bound", tn.test_roundtrip_bound_and_exact_dequant),
+    ("nvfp4 special", tn.test_special_blocks),
 ]
+if tn.HAS_F8:
+    PINS += [("e4m3 torch decode", tn.test_e4m3_decode_matches_torch),
+             ("e4m3 torch encode", tn.test_e4m3_encode_matches_torch_in_range)]
 
 MUTANTS = {
     "nibble_order": ("if (v & 1) qr[v >> 1]", "if (!(v & 1)) qr[v >> 1]"),
@@ -34,9 +45,17 @@ MUTANTS = {
     "scale_divisor": ("float s = amax / (float)qmax;", "float s = amax / (float)(qmax + 1);"),
     "round_half_away": ("float r = nearbyintf(x / d);", "float r = roundf(x / d);"),
     "no_saturation": ("if (d == 0x7C00u) d = 0x7BFFu;", ""),
-    "q8_group": ("return codec == ORC_Q4 ? 64 : 32;", "return codec == ORC_Q4 ? 64 : 64;"),
-    "q4_g32_group": ("static int orc_group(int codec) { return codec == ORC_Q4 ? 64 : 32; }",
-                     "static int orc_group(int codec) { return (codec == ORC_Q4 || codec == ORC_Q4_32) ? 64 : 32; }"),
+    "q8_group": ("codec == ORC_NVFP4 ? 16 : 32; }", "codec == ORC_NVFP4 ? 16 : 64; }"),
+    "q4_g32_group": ("static int orc_group(int codec) { return codec == ORC_Q4 ? 64 :",
+                     "static int orc_group(int codec) { return (codec == ORC_Q4 || codec == ORC_Q4_32) ? 64 :"),
+    "nvfp4_scale_divisor": ("uint8_t sb = orc_f32_to_e4m3(amax / 6.0f);", "uint8_t sb = orc_f32_to_e4m3(amax / 7.0f);"),
+    "fp8_ties_up": ("if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {", "if (d <= bd) {"),
+    "fp8_no_saturation": ("    if (a >= decode((uint8_t)(n_codes - 1))) return n_codes - 1;\n", ""),
+    "e4m3_bias": ("else v = (1.0f + (float)m / 8.0f) * ldexpf(1.0f, e - 7);",
+                  "else v = (1.0f + (float)m / 8.0f) * ldexpf(1.0f, e - 8);"),
+    "e2m1_zero_sign_dropped": ("return (uint8_t)(c | (signbit(f) ? 8 : 0));",
+                               "return (uint8_t)(c | (c != 0 && signbit(f) ? 8 : 0));"),
+    "nvfp4_zero_scale": ("c[i] = (d == 0.0f) ? 0 : orc_f32_to_e2m1(x[i] / d);", "c[i] = orc_f32_to_e2m1(x[i] / d);"),
     "f16_truncates": ("if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;", ""),
     "f16_subnormal_shift": ("uint32_t shift = 126u - e;", "uint32_t shift = 127u - e;"),
     "gqa_mapping": ("int r = i * G + j, h = kh * G + j;", "int r = i * G + j, h = kh + j * a->n_kv_heads;"),

@@ -43,6 +43,7 @@ import numpy as np
 Q4_G64 = 1
 Q8_0 = 2
 Q4_G32 = 3
+NVFP4 = 4                 # E2M1 values, one E4M3 scale per 16
 BASE_SEED = 20261202
 TOKEN_ALIGN = 64          # cache capacity is a multiple of this many tokens
 
@@ -177,8 +178,10 @@ def custom(name="custom", n_seq=1, n_heads=1, n_kv_heads=1, head_dim=128, cached
 
 
 def kv_bytes_per_token(sp: Spec) -> int:
-    """Packed K + V bytes of one token over all kv heads (codes + fp16 scales)."""
+    """Packed K + V bytes of one token over all kv heads (codes + scales)."""
     def row(codec):
+        if codec == NVFP4:
+            return sp.head_dim // 2 + sp.head_dim // 16
         if codec == Q4_G64:
             return sp.head_dim // 2 + 2 * (sp.head_dim // 64)
         if codec == Q4_G32:
