@@ -67,8 +67,24 @@ typedef enum kvq_status {
  *   pair; "Results": the 65K serve run), whose format the pages do not give:
  *   the Q4_G64 rule and code layout with groups of 32 values (head_dim/32
  *   scales, 4.5 bits per value).  Not llama.cpp's q4_0 byte layout.
- * Dequantized value = (float)scale * code, exact in fp32. */
-typedef enum kvq_codec { KVQ_CODEC_Q4_G64 = 1, KVQ_CODEC_Q8_0 = 2, KVQ_CODEC_Q4_G32 = 3 } kvq_codec;
+ * KVQ_CODEC_NVFP4 -- the NVFP4 KV type of the "-ctk nvfp4 -ctv nvfp4" and
+ *   "-ctk q8_0 -ctv nvfp4" runs (den_llama.cpp, "What this fork is";
+ *   "build3 (working engine) -- additions", NVFP4 KV row), whose format the
+ *   pages do not give: NVIDIA's published NVFP4 without its per-tensor scale.
+ *   Per block of 16 values: scale = E4M3(absmax / 6) (fp32 quotient; FP8
+ *   E4M3: bias 7, 3 mantissa bits, largest finite 448), code = E2M1(x /
+ *   (float)scale) (FP4 E2M1: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, sign in
+ *   bit 3, a negative value that rounds to 0 keeps its sign), both rounded to
+ *   nearest, ties to even, and held at the largest finite value; codes 0 when
+ *   the scale is 0.  A row is head_dim/2 code bytes (Q4_G64's nibble order)
+ *   plus head_dim/16 one-byte E4M3 scales (4.5 bits per value).
+ * Dequantized value = (float)scale * code value, exact in fp32. */
+typedef enum kvq_codec {
+    KVQ_CODEC_Q4_G64 = 1,
+    KVQ_CODEC_Q8_0 = 2,
+    KVQ_CODEC_Q4_G32 = 3,
+    KVQ_CODEC_NVFP4 = 4
+} kvq_codec;
 
 typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_F16 = 1 } kvq_dtype;
 
@@ -82,7 +98,8 @@ typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_F16 = 1 } kvq_dtype;
 
 /* One layer's K (or V) cache: two planes, both in device memory.
  *   qs     : code bytes, [n_seq][n_kv_heads][capacity][kvq_row_bytes(codec, head_dim)]
- *   scales : fp16 scales, [n_seq][n_kv_heads][capacity][kvq_scales_per_row(codec, head_dim)]
+ *   scales : [n_seq][n_kv_heads][capacity][kvq_scales_per_row(codec, head_dim)] scales
+ *            of kvq_scale_bytes(codec) bytes each (fp16; E4M3 bytes for NVFP4)
  * Both planes are 16-byte aligned.  head_dim is a multiple of 64 in
  * [64, 512]; capacity is a positive multiple of KVQ_CAPACITY_ALIGN. */
 typedef struct kvq_cache {
@@ -97,8 +114,10 @@ typedef struct kvq_cache {
 
 /* Bytes of one row of the code plane, or 0 for an unknown codec. */
 int32_t kvq_row_bytes(int32_t codec, int32_t head_dim);
-/* FP16 scales in one row, or 0 for an unknown codec. */
+/* Scales in one row, or 0 for an unknown codec. */
 int32_t kvq_scales_per_row(int32_t codec, int32_t head_dim);
+/* Bytes of one scale (2: fp16; 1: E4M3 for NVFP4), or 0 for an unknown codec. */
+int32_t kvq_scale_bytes(int32_t codec);
 
 /* Quantize-on-append (the KV-cache append stage).
  *   k_src, v_src : DEVICE, [n_seq][n_new][n_kv_heads][head_dim], dtype src_dtype

@@ -18,6 +18,7 @@ KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE, KVQ_ECUDA = range(5)
 KVQ_CODEC_Q4_G64 = 1
 KVQ_CODEC_Q8_0 = 2
 KVQ_CODEC_Q4_G32 = 3
+KVQ_CODEC_NVFP4 = 4
 KVQ_F32, KVQ_F16 = 0, 1
 KVQ_ERR_APPEND_POS, KVQ_ERR_KV_LEN, KVQ_ERR_TIMEOUT = 1, 2, 4
 KVQ_CAPACITY_ALIGN = 64
@@ -48,6 +49,7 @@ def _load():
     sig = {
         "kvq_row_bytes": (I32, [I32, I32]),
         "kvq_scales_per_row": (I32, [I32, I32]),
+        "kvq_scale_bytes": (I32, [I32]),
         "kvq_quantize_append": (I32, [C, C, P, P, I32, I32, P, P, P]),
         "kvq_decode_default_splits": (I32, [C, C, I32, I32, I32]),
         "kvq_decode_workspace_bytes": (SZ, [C, C, I32, I32, I32, I32]),
@@ -66,7 +68,7 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("kvq_row_bytes", "kvq_scales_per_row", "kvq_quantize_append", "kvq_decode_default_splits",
+EXPORTED = ("kvq_row_bytes", "kvq_scales_per_row", "kvq_scale_bytes", "kvq_quantize_append", "kvq_decode_default_splits",
             "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_merge_splits", "kvq_dequantize",
             "kvq_status_string", "kvq_last_error", "kvq_static_scratch_bytes", "kvq_decode_attention_static")
 
@@ -100,9 +102,14 @@ def kvq_scales_per_row(codec: int, head_dim: int) -> int:
     return int(_lib.kvq_scales_per_row(codec, head_dim))
 
 
+def kvq_scale_bytes(codec: int) -> int:
+    return int(_lib.kvq_scale_bytes(codec))
+
+
 class KVCache:
-    """One layer's K or V cache in device memory: qs uint8 and scales fp16 planes,
-    [n_seq][n_kv_heads][capacity][...] (layout as in include/kvq.h)."""
+    """One layer's K or V cache in device memory: a qs uint8 plane and a scales
+    plane (fp16; uint8 E4M3 for NVFP4), [n_seq][n_kv_heads][capacity][...]
+    (layout as in include/kvq.h)."""
 
     def __init__(self, codec, n_seq, n_kv_heads, head_dim, capacity, device="cuda", qs=None, scales=None):
         self.codec, self.n_seq, self.n_kv_heads = int(codec), int(n_seq), int(n_kv_heads)
@@ -110,7 +117,8 @@ class KVCache:
         rb, ns = kvq_row_bytes(codec, head_dim), kvq_scales_per_row(codec, head_dim)
         shape = (self.n_seq, self.n_kv_heads, self.capacity)
         self.qs = qs if qs is not None else torch.zeros(shape + (rb,), dtype=torch.uint8, device=device)
-        self.scales = scales if scales is not None else torch.zeros(shape + (ns,), dtype=torch.float16, device=device)
+        sdt = torch.uint8 if kvq_scale_bytes(codec) == 1 else torch.float16
+        self.scales = scales if scales is not None else torch.zeros(shape + (ns,), dtype=sdt, device=device)
         self._c = kvq_cache(self.codec, self.n_seq, self.n_kv_heads, self.head_dim, self.capacity,
                             self.qs.data_ptr(), self.scales.data_ptr())
 
@@ -119,7 +127,7 @@ class KVCache:
         return ctypes.byref(self._c)
 
     def nbytes(self) -> int:
-        return self.qs.numel() + 2 * self.scales.numel()
+        return self.qs.numel() + self.scales.numel() * self.scales.element_size()
 
     def seq_view(self, s: int) -> "KVCache":
         """The planes of sequence s alone, as a one-sequence cache (shares memory)."""

@@ -29,7 +29,10 @@ kvq_status cuda_status(cudaError_t e, const char *what)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool valid_codec(int32_t c) { return c == KVQ_CODEC_Q4_G64 || c == KVQ_CODEC_Q8_0 || c == KVQ_CODEC_Q4_G32; }
+bool valid_codec(int32_t c)
+{
+    return c == KVQ_CODEC_Q4_G64 || c == KVQ_CODEC_Q8_0 || c == KVQ_CODEC_Q4_G32 || c == KVQ_CODEC_NVFP4;
+}
 
 bool valid_head_dim(int32_t d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
@@ -54,7 +57,7 @@ kvq_status check_cache(const kvq_cache *c, const char *name)
 
 kvq::Plane plane_of(const kvq_cache *c)
 {
-    return kvq::Plane{c->codec, static_cast<uint8_t *>(c->qs), static_cast<__half *>(c->scales)};
+    return kvq::Plane{c->codec, static_cast<uint8_t *>(c->qs), static_cast<uint8_t *>(c->scales)};
 }
 
 int sm_count()
@@ -122,6 +125,11 @@ int32_t kvq_row_bytes(int32_t codec, int32_t head_dim)
 int32_t kvq_scales_per_row(int32_t codec, int32_t head_dim)
 {
     return valid_codec(codec) ? kvq::scales_per_row(codec, head_dim) : 0;
+}
+
+int32_t kvq_scale_bytes(int32_t codec)
+{
+    return valid_codec(codec) ? kvq::scale_bytes(codec) : 0;
 }
 
 const char *kvq_status_string(int32_t status)

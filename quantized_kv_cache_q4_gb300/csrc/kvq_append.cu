@@ -1,15 +1,20 @@
-// kvq_append.cu -- quantize-on-append: new K/V rows are quantized to Q4_G64 or
-// q8_0 and written at their cache positions (den_llama.cpp, "What's in the
-// fork": the set-rows / cpy-utils quantize path of the Q4_G64 codec; the codec
-// itself in "What this fork is": signed INT4 + one FP16 scale per 64 values).
+// kvq_append.cu -- quantize-on-append: new K/V rows are quantized to Q4_G64,
+// Q4_G32, q8_0 or NVFP4 and written at their cache positions (den_llama.cpp,
+// "What's in the fork": the set-rows / cpy-utils quantize path of the Q4_G64
+// codec; the codec itself in "What this fork is": signed INT4 + one FP16
+// scale per 64 values; the NVFP4 KV type of the same section, read as
+// NVIDIA's published NVFP4).
 //
 // One warp quantizes one (plane, sequence, new token, kv head) row.  Lane l
 // owns the VPL = head_dim/32 consecutive values [l*VPL, (l+1)*VPL); a group of
-// 64 (Q4_G64) or 32 (q8_0) values is then 64/VPL or 32/VPL aligned lanes whose
-// absmax is combined with xor-shuffles.  The arithmetic is the codec rule
-// itself: scale = fp16_rne(absmax / qmax) via IEEE division (__fdiv_rn),
-// saturated to 65504; code = clamp(rne(x / (float)scale)) via IEEE division and
-// round-to-nearest-even conversion.  This TU must not be built with fast-math.
+// 64 (Q4_G64), 32 (Q4_G32, q8_0) or 16 (NVFP4) values is then group/VPL
+// aligned lanes whose absmax is combined with xor-shuffles.  The arithmetic is
+// the codec rule itself: scale = fp16_rne(absmax / qmax) via IEEE division
+// (__fdiv_rn), saturated to 65504; code = clamp(rne(x / (float)scale)) via
+// IEEE division and round-to-nearest-even conversion.  NVFP4: scale =
+// E4M3(absmax / 6), code = E2M1(x / scale), the hardware's round-to-nearest-
+// even saturating conversions, the code's sign bit set from the value's.  This
+// TU must not be built with fast-math.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -113,7 +118,39 @@ __device__ __forceinline__ void store_q4(const Plane &P, int64_t crow, int lane,
         else hi |= nib << (4 * (v - 16));
     }
     store_bytes<VPL / 2>(P.qs + crow * (D / 2) + lane * (VPL / 2), lo, hi);
-    if (lane % LPG == 0) P.sc[crow * (D / GS) + lane / LPG] = hs;
+    if (lane % LPG == 0) reinterpret_cast<__half *>(P.sc)[crow * (D / GS) + lane / LPG] = hs;
+}
+
+// NVFP4: blocks of 16 values (16 / VPL aligned lanes).  The block's absmax / 6
+// (IEEE division) to E4M3 (cvt.rn.satfinite), then each value divided by the
+// decoded scale (IEEE) to E2M1 (cvt.rn.satfinite), two codes per byte, the
+// sign bits taken from the values so that a negative value rounding to 0 is
+// -0 whatever the converter does with it; all codes 0 when the scale is 0.
+template <int VPL>
+__device__ __forceinline__ void store_fp4(const Plane &P, int64_t crow, int lane, const float (&x)[VPL], float amax)
+{
+    constexpr int D = VPL * 32;
+    constexpr int LPG = 16 / VPL;
+#pragma unroll
+    for (int off = 1; off < LPG; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    unsigned short e16;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(e16) : "f"(0.0f), "f"(__fdiv_rn(amax, 6.0f)));
+    const uint32_t sb = e16 & 0xFFu;
+    const float d = e4m3_to_float(sb);
+    uint64_t lo = 0, hi = 0;
+    if (d != 0.0f) {
+#pragma unroll
+        for (int v = 0; v < VPL; v += 2) {
+            uint32_t b;
+            asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+                : "=r"(b) : "f"(__fdiv_rn(x[v + 1], d)), "f"(__fdiv_rn(x[v], d)));
+            b = (b & 0x77u) | (signbit(x[v]) ? 0x08u : 0u) | (signbit(x[v + 1]) ? 0x80u : 0u);
+            if (v < 16) lo |= (uint64_t)b << (4 * v);
+            else hi |= (uint64_t)b << (4 * (v - 16));
+        }
+    }
+    store_bytes<VPL / 2>(P.qs + crow * (D / 2) + lane * (VPL / 2), lo, hi);
+    if (lane % LPG == 0) P.sc[crow * (D / 16) + lane / LPG] = (uint8_t)sb;
 }
 
 template <int VPL, typename SrcT>
@@ -152,6 +189,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
         store_q4<VPL, 64>(P, crow, lane, x, amax);
     } else if (P.codec == KVQ_CODEC_Q4_G32) {
         store_q4<VPL, 32>(P, crow, lane, x, amax);
+    } else if (P.codec == KVQ_CODEC_NVFP4) {
+        store_fp4<VPL>(P, crow, lane, x, amax);
     } else {
         constexpr int LPG = 32 / VPL;
         const __half hs = group_scale<LPG>(amax, 127.0f);
@@ -164,7 +203,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
             else hi |= b << (8 * (v - 8));
         }
         store_bytes<VPL>(P.qs + crow * D + lane * VPL, lo, hi);
-        if (lane % LPG == 0) P.sc[crow * (D / 32) + lane / LPG] = hs;
+        if (lane % LPG == 0) reinterpret_cast<__half *>(P.sc)[crow * (D / 32) + lane / LPG] = hs;
     }
 }
 
@@ -205,8 +244,19 @@ __global__ void dequant_kernel(Plane p, int64_t n_rows, int head_dim, float *out
     const int64_t r = idx / per_row;
     const int v0 = (int)(idx % per_row) * 8;
     const int gs = group_size(p.codec);
-    const float d = __half2float(p.sc[r * (head_dim / gs) + v0 / gs]);
     float *o = out + r * head_dim + v0;
+    if (is_fp4(p.codec)) {
+        const float d = e4m3_to_float(p.sc[r * (head_dim / 16) + v0 / 16]);
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(p.qs + r * (head_dim / 2) + v0 / 2);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t h2 = e2m1x2_to_h2(w >> (8 * j));
+            o[2 * j] = d * __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+            o[2 * j + 1] = d * __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+        }
+        return;
+    }
+    const float d = __half2float(reinterpret_cast<const __half *>(p.sc)[r * (head_dim / gs) + v0 / gs]);
     if (is_q4(p.codec)) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(p.qs + r * (head_dim / 2) + v0 / 2);
 #pragma unroll

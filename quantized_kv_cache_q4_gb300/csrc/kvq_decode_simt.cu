@@ -39,11 +39,20 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// N consecutive codes starting at value index v0 of a row (v0 a multiple of N).
+// The values of N consecutive codes starting at value index v0 of a row (v0 a
+// multiple of N): the integer codes, or NVFP4's E2M1 values.
 template <int CODEC, int N>
-__device__ __forceinline__ void load_codes(const uint8_t *row, int v0, int (&c)[N])
+__device__ __forceinline__ void load_codes(const uint8_t *row, int v0, float (&c)[N])
 {
-    if constexpr (is_q4(CODEC)) {
+    if constexpr (is_fp4(CODEC)) {
+        const uint8_t *p = row + v0 / 2;
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+            const uint32_t h2 = e2m1x2_to_h2(p[j]);
+            c[2 * j] = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+            c[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+        }
+    } else if constexpr (is_q4(CODEC)) {
         const uint8_t *p = row + v0 / 2;
         uint64_t w;
         if constexpr (N == 2) w = *p;
@@ -56,12 +65,12 @@ __device__ __forceinline__ void load_codes(const uint8_t *row, int v0, int (&c)[
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             int nib = (int)((w >> (4 * j)) & 0xF);
-            c[j] = nib >= 8 ? nib - 16 : nib;
+            c[j] = (float)(nib >= 8 ? nib - 16 : nib);
         }
     } else {
         const uint8_t *p = row + v0;
 #pragma unroll
-        for (int j = 0; j < N; ++j) c[j] = (int)(int8_t)p[j];
+        for (int j = 0; j < N; ++j) c[j] = (float)(int8_t)p[j];
     }
 }
 
@@ -100,9 +109,10 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
 
     const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
     const uint8_t *kqs = a.k.qs + plane_row * KRB;
-    const __half *ksc = a.k.sc + plane_row * (D / KG);
+    constexpr int KSR = scale_row_bytes(KC, D), VSR = scale_row_bytes(VC, D);
+    const uint8_t *ksc = a.k.sc + plane_row * KSR;
     const uint8_t *vqs = a.v.qs + plane_row * VRB;
-    const __half *vsc = a.v.sc + plane_row * (D / VG);
+    const uint8_t *vsc = a.v.sc + plane_row * VSR;
     const QT *q = static_cast<const QT *>(a.q);
     const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
 
@@ -145,17 +155,17 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
                 const uint8_t *krow = kqs + (int64_t)t * KRB;
 #pragma unroll 1
                 for (int g = 0; g < D / KG; ++g) {
-                    const float dsc = __half2float(ksc[(int64_t)t * (D / KG) + g]);
+                    const float dsc = load_scale<KC>(ksc + (int64_t)t * KSR, g);
                     float part[RB];
 #pragma unroll
                     for (int r = 0; r < RB; ++r) part[r] = 0.0f;
 #pragma unroll 1
                     for (int v0 = g * KG; v0 < (g + 1) * KG; v0 += 8) {
-                        int c[8];
+                        float c[8];
                         load_codes<KC, 8>(krow, v0, c);
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
-                            const float cf = (float)c[jj];
+                            const float cf = c[jj];
 #pragma unroll
                             for (int r = 0; r < RB; ++r) part[r] = fmaf(qf[r][v0 + jj], cf, part[r]);
                         }
@@ -181,14 +191,14 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
 #pragma unroll 1
             for (int j = 0; j < nt; ++j) {
                 const int tj = tb + j;
-                int c[VPL];
+                float c[VPL];
                 load_codes<VC, VPL>(vqs + (int64_t)tj * VRB, lane * VPL, c);
-                const float dsc = __half2float(vsc[(int64_t)tj * (D / VG) + (lane * VPL) / VG]);
+                const float dsc = load_scale<VC>(vsc + (int64_t)tj * VSR, (lane * VPL) / VG);
 #pragma unroll
                 for (int r = 0; r < RB; ++r) {
                     const float p = pbuf[warp][j][r];
 #pragma unroll
-                    for (int v = 0; v < VPL; ++v) o[r][v] = fmaf(p, dsc * (float)c[v], o[r][v]);
+                    for (int v = 0; v < VPL; ++v) o[r][v] = fmaf(p, dsc * c[v], o[r][v]);
                 }
             }
             __syncwarp();
@@ -269,6 +279,7 @@ cudaError_t launch_v(const DecodeArgs &a, int q_dtype, cudaStream_t st)
     case KVQ_CODEC_Q4_G64: return launch2<KC, KVQ_CODEC_Q4_G64>(a, q_dtype, st);
     case KVQ_CODEC_Q8_0: return launch2<KC, KVQ_CODEC_Q8_0>(a, q_dtype, st);
     case KVQ_CODEC_Q4_G32: return launch2<KC, KVQ_CODEC_Q4_G32>(a, q_dtype, st);
+    case KVQ_CODEC_NVFP4: return launch2<KC, KVQ_CODEC_NVFP4>(a, q_dtype, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -281,6 +292,7 @@ cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st
     case KVQ_CODEC_Q4_G64: return launch_v<KVQ_CODEC_Q4_G64>(a, q_dtype, st);
     case KVQ_CODEC_Q8_0: return launch_v<KVQ_CODEC_Q8_0>(a, q_dtype, st);
     case KVQ_CODEC_Q4_G32: return launch_v<KVQ_CODEC_Q4_G32>(a, q_dtype, st);
+    case KVQ_CODEC_NVFP4: return launch_v<KVQ_CODEC_NVFP4>(a, q_dtype, st);
     default: return cudaErrorInvalidValue;
     }
 }

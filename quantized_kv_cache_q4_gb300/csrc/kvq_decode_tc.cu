@@ -8,7 +8,7 @@ bool decode_tc_supported(const DecodeArgs &a)
 {
     const int R = a.n_q * (a.n_heads / a.n_kv_heads);
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
-    return R >= 1 && R <= 32 &&
+    return R >= 1 && R <= 32 && !is_fp4(a.k.codec) &&
            (a.v.codec == KVQ_CODEC_Q4_G64 || a.v.codec == KVQ_CODEC_Q4_G32 || a.v.codec == KVQ_CODEC_Q8_0) &&
            (a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256) && rows < (1LL << 31) &&
            tensor_maps_available();

@@ -16,11 +16,20 @@ constexpr int kWarp = 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// 4-bit codecs (Q4_G64, Q4_G32) share the code layout; q8_0 has one byte per value.
+// The 4-bit integer codecs (Q4_G64, Q4_G32) and NVFP4 (E2M1 codes) store two
+// codes per byte (value 2j in the low nibble); q8_0 one per byte.  Scales are
+// fp16, except NVFP4's one E4M3 byte per 16 values.
 __host__ __device__ constexpr bool is_q4(int codec) { return codec == KVQ_CODEC_Q4_G64 || codec == KVQ_CODEC_Q4_G32; }
-__host__ __device__ constexpr int group_size(int codec) { return codec == KVQ_CODEC_Q4_G64 ? 64 : 32; }
-__host__ __device__ constexpr int row_bytes(int codec, int d) { return is_q4(codec) ? d / 2 : d; }
+__host__ __device__ constexpr bool is_fp4(int codec) { return codec == KVQ_CODEC_NVFP4; }
+__host__ __device__ constexpr bool two_per_byte(int codec) { return is_q4(codec) || is_fp4(codec); }
+__host__ __device__ constexpr int group_size(int codec)
+{
+    return codec == KVQ_CODEC_Q4_G64 ? 64 : codec == KVQ_CODEC_NVFP4 ? 16 : 32;
+}
+__host__ __device__ constexpr int row_bytes(int codec, int d) { return two_per_byte(codec) ? d / 2 : d; }
 __host__ __device__ constexpr int scales_per_row(int codec, int d) { return d / group_size(codec); }
+__host__ __device__ constexpr int scale_bytes(int codec) { return is_fp4(codec) ? 1 : 2; }
+__host__ __device__ constexpr int scale_row_bytes(int codec, int d) { return scales_per_row(codec, d) * scale_bytes(codec); }
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch: a kernel launched with launch_pdl() may start
@@ -48,11 +57,35 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// A cache plane as the kernels see it.
+// Hardware conversions (exact): an E4M3 byte to fp32; a byte of two E2M1
+// codes to fp16x2 bits (low nibble -> low half).
+__device__ __forceinline__ float e4m3_to_float(uint32_t b)
+{
+    uint32_t h2;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(b & 0xFFu));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte)
+{
+    uint32_t h2;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte & 0xFFu));
+    return h2;
+}
+
+// One scale of a plane row as fp32.
+template <int CODEC>
+__device__ __forceinline__ float load_scale(const uint8_t *row_scales, int g)
+{
+    if constexpr (is_fp4(CODEC)) return e4m3_to_float(row_scales[g]);
+    else return __half2float(reinterpret_cast<const __half *>(row_scales)[g]);
+}
+
+// A cache plane as the kernels see it (sc: the scale plane as bytes).
 struct Plane {
     int codec;
     uint8_t *qs;
-    __half *sc;
+    uint8_t *sc;
 };
 
 struct AppendArgs {

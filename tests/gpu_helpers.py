@@ -32,6 +32,10 @@ def gpu_caches(wl: workloads.Workload, append=True):
 
 
 def host_planes(c: kvq.KVCache):
+    """The planes as the oracle holds them: codes uint8, scales uint16 fp16 bit
+    patterns (uint8 E4M3 bytes for NVFP4)."""
+    if c.scales.dtype == torch.uint8:
+        return c.qs.cpu().numpy(), c.scales.cpu().numpy()
     return c.qs.cpu().numpy(), c.scales.cpu().view(torch.int16).numpy().view(np.uint16)
 
 

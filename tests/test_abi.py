@@ -34,11 +34,16 @@ def test_row_sizes():
     assert kvq.kvq_scales_per_row(kvq.KVQ_CODEC_Q8_0, 256) == 8
     assert kvq.kvq_row_bytes(kvq.KVQ_CODEC_Q4_G32, 256) == 128
     assert kvq.kvq_scales_per_row(kvq.KVQ_CODEC_Q4_G32, 256) == 8
+    assert kvq.kvq_row_bytes(kvq.KVQ_CODEC_NVFP4, 256) == 128
+    assert kvq.kvq_scales_per_row(kvq.KVQ_CODEC_NVFP4, 256) == 16
     assert kvq.kvq_row_bytes(99, 256) == 0
-    # 4.25, 8.5 and 4.5 bits per value
-    for codec, bits in ((kvq.KVQ_CODEC_Q4_G64, 4.25), (kvq.KVQ_CODEC_Q8_0, 8.5), (kvq.KVQ_CODEC_Q4_G32, 4.5)):
+    assert [kvq.kvq_scale_bytes(c) for c in (1, 2, 3, 4, 99)] == [2, 2, 2, 1, 0]
+    # 4.25, 8.5, 4.5 and 4.5 bits per value
+    for codec, bits in ((kvq.KVQ_CODEC_Q4_G64, 4.25), (kvq.KVQ_CODEC_Q8_0, 8.5), (kvq.KVQ_CODEC_Q4_G32, 4.5),
+                        (kvq.KVQ_CODEC_NVFP4, 4.5)):
         for d in (64, 128, 256, 512):
-            assert (kvq.kvq_row_bytes(codec, d) + 2 * kvq.kvq_scales_per_row(codec, d)) * 8 == bits * d
+            sb = kvq.kvq_scale_bytes(codec)
+            assert (kvq.kvq_row_bytes(codec, d) + sb * kvq.kvq_scales_per_row(codec, d)) * 8 == bits * d
 
 
 def _fake_cache(**kw):
@@ -54,7 +59,7 @@ def _append(k, v, ksrc=4096, vsrc=4096, dtype=kvq.KVQ_F16, n_new=1, pos=4096):
 
 
 @pytest.mark.parametrize("bad,status", [
-    (dict(codec=4), kvq.KVQ_EINVAL), (dict(codec=0), kvq.KVQ_EINVAL), (dict(head_dim=96), kvq.KVQ_EINVAL), (dict(head_dim=1024), kvq.KVQ_EINVAL),
+    (dict(codec=5), kvq.KVQ_EINVAL), (dict(codec=0), kvq.KVQ_EINVAL), (dict(head_dim=96), kvq.KVQ_EINVAL), (dict(head_dim=1024), kvq.KVQ_EINVAL),
     (dict(capacity=100), kvq.KVQ_EINVAL), (dict(capacity=0), kvq.KVQ_EINVAL), (dict(n_seq=0), kvq.KVQ_EINVAL),
     (dict(qs=0), kvq.KVQ_EINVAL), (dict(qs=4097), kvq.KVQ_EINVAL), (dict(scales=8200), kvq.KVQ_EINVAL),
     (dict(head_dim=192), kvq.KVQ_EUNSUPPORTED)])

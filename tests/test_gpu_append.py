@@ -27,7 +27,8 @@ def test_workload_caches_byte_exact(cfg):
             assert np.array_equal(sc[s, :, :n], o.scales[s, :, :n])
 
 
-@pytest.mark.parametrize("codec", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32])
+@pytest.mark.parametrize("codec", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32,
+                                   kvq.KVQ_CODEC_NVFP4])
 @pytest.mark.parametrize("D", [64, 128, 256, 512])
 @pytest.mark.parametrize("dtype", [np.float32, np.float16])
 def test_wide_range_rows_byte_exact(codec, D, dtype):

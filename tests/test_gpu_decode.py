@@ -61,7 +61,9 @@ def test_split_counts(n_splits):
 
 @pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0),
                                    (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32),
-                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32), (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0)])
+                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32), (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0),
+                                   (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_NVFP4),
+                                   (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_Q4_G64)])
 @pytest.mark.parametrize("D", [128, 256, 512])
 def test_codec_pairs(kc, vc, D):
     wl = workloads.custom(n_seq=2, n_heads=8, n_kv_heads=2, head_dim=D, cached=(700, 333), n_new=1, k_codec=kc,
@@ -92,7 +94,7 @@ def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
 
 
 @pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q8_0),
-                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32)])
+                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32), (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4)])
 @pytest.mark.parametrize("D", [128, 256])
 def test_more_than_32_rows_per_kv_head(kc, vc, D):
     """12 query heads per kv head x 3 query tokens = 36 rows: past the
@@ -102,6 +104,24 @@ def test_more_than_32_rows_per_kv_head(kc, vc, D):
     k, v, ko, vo = _both(wl)
     o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
     for n_splits in (0, 2):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_NVFP4),
+                                   (kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_NVFP4)])
+@pytest.mark.parametrize("G,n_new", [(1, 1), (6, 3), (8, 4)])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_nvfp4_pairs(kc, vc, G, n_new, D):
+    """NVFP4 caches (the pages' NVFP4 KV type), K and V, at 1..32 rows per kv
+    head, outlier values (scales over a wide range) and a ragged last tile."""
+    wl = workloads.custom(n_seq=2, n_heads=2 * G, n_kv_heads=2, head_dim=D, cached=(700 - n_new, 97), n_new=n_new,
+                          k_codec=kc, v_codec=vc, src_dtype="f16", q_dtype="f16", dist="outliers",
+                          seed=13 * kc + 7 * vc + G + D)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (0, 3):
         o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
         assert err == 0
         check_close(o, o_ref, lse, lse_ref)
