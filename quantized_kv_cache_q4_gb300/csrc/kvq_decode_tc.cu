@@ -1,5 +1,5 @@
 // kvq_decode_tc.cu -- the tensor-core decode kernel (kvq_decode_tc.cuh) for V
-// in Q4_G64, and the dispatch of the three V codecs.
+// in Q4_G64, and the dispatch of the four V codecs.
 #include "kvq_decode_tc.cuh"
 
 namespace kvq {
@@ -8,8 +8,7 @@ bool decode_tc_supported(const DecodeArgs &a)
 {
     const int R = a.n_q * (a.n_heads / a.n_kv_heads);
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
-    return R >= 1 && R <= 32 && !is_fp4(a.k.codec) &&
-           (a.v.codec == KVQ_CODEC_Q4_G64 || a.v.codec == KVQ_CODEC_Q4_G32 || a.v.codec == KVQ_CODEC_Q8_0) &&
+    return R >= 1 && R <= 32 &&
            (a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256) && rows < (1LL << 31) &&
            tensor_maps_available();
 }
@@ -21,6 +20,7 @@ int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_h
     if (v_codec == KVQ_CODEC_Q4_G64) return per_sm_for_v<KVQ_CODEC_Q4_G64>(k_codec, head_dim, nt);
     if (v_codec == KVQ_CODEC_Q4_G32) return decode_tc_g32_ctas_per_sm(k_codec, head_dim, nt);
     if (v_codec == KVQ_CODEC_Q8_0) return decode_tc_q8v_ctas_per_sm(k_codec, head_dim, nt);
+    if (v_codec == KVQ_CODEC_NVFP4) return decode_tc_fp4v_ctas_per_sm(k_codec, head_dim, nt);
     return 0;
 }
 
@@ -29,6 +29,7 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st)
     if (a.v.codec == KVQ_CODEC_Q4_G64) return launch_for_v<KVQ_CODEC_Q4_G64>(a, q_dtype, st);
     if (a.v.codec == KVQ_CODEC_Q4_G32) return launch_decode_tc_g32(a, q_dtype, st);
     if (a.v.codec == KVQ_CODEC_Q8_0) return launch_decode_tc_q8v(a, q_dtype, st);
+    if (a.v.codec == KVQ_CODEC_NVFP4) return launch_decode_tc_fp4v(a, q_dtype, st);
     return cudaErrorInvalidValue;
 }
 

@@ -1,9 +1,12 @@
 // kvq_decode_tc.cuh -- split-K decode / MTP-verify attention over a packed cache
 // on the tensor cores, for 1..32 query rows per kv head (GQA group x query
-// tokens), head_dim 64/128/256, K and V each in Q4_G64, Q4_G32 or q8_0 (the
-// kernel template; kvq_decode_tc.cu, kvq_decode_tc_g32.cu and
-// kvq_decode_tc_q8v.cu hold its instances for the three V codecs, so that
-// they compile in parallel)
+// tokens), head_dim 64/128/256, K and V each in Q4_G64, Q4_G32, q8_0 or
+// NVFP4 (the kernel template; kvq_decode_tc.cu, kvq_decode_tc_g32.cu,
+// kvq_decode_tc_q8v.cu and kvq_decode_tc_fp4v.cu hold its instances for the
+// four V codecs, so that they compile in parallel).  NVFP4 codes enter the
+// MMAs as exact fp16 values already multiplied by their E4M3 scales (an E2M1
+// value times an E4M3 scale has at most 6 significant bits), so they need no
+// bias, offset or per-group scaling of the accumulators.
 // (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
 // this fork is": signed INT4 + one FP16 scale per 64 values; "Results": MTP
 // n-max 2, i.e. 1 + 2 query tokens per sequence).
@@ -60,8 +63,11 @@ __device__ __forceinline__ void warps_sync() { asm volatile("bar.sync 1, %0;" ::
 template <int KC, int VC, int D, int NT, typename QT>
 struct TcCfg {
     static constexpr int KRB = row_bytes(KC, D), VRB = row_bytes(VC, D);
-    static constexpr int KSB = 2 * scales_per_row(KC, D), VSB = 2 * scales_per_row(VC, D);
-    static constexpr int NGK = D / group_size(KC);
+    static constexpr int KSB = scale_row_bytes(KC, D), VSB = scale_row_bytes(VC, D);
+    // K accumulation groups: the codec's scale groups, or for NVFP4 (scales
+    // applied to the operands) the 64 values of one ldmatrix unit
+    static constexpr int KGS = is_fp4(KC) ? 64 : group_size(KC);
+    static constexpr int NGK = D / KGS;
     static constexpr int ROWS = NT * 8;                           // query rows kept (zero past R)
     static constexpr int PS = ROWS + 4;                           // score row stride in floats (bank spread)
     static constexpr int K_OFF = 0;
@@ -103,6 +109,8 @@ __device__ __forceinline__ int kpos_to_d(int ks, int kp)
     // Q4_G32: both k-steps of a group come from its one 16-byte chunk (nibble
     // pairs 2 sub / 2 sub + 1 for the two k halves)
     else if constexpr (KC == KVQ_CODEC_Q4_G32) return 32 * (ks >> 1) + 8 * t + 2 * (ks & 1) + hi + 4 * h;
+    // NVFP4: byte e of a 4-byte piece converts to the pair (2e, 2e + 1)
+    else if constexpr (KC == KVQ_CODEC_NVFP4) return 64 * (ks >> 2) + 32 * hi + 8 * t + 2 * (ks & 3) + h;
     else return 32 * (ks >> 1) + 16 * hi + 4 * t + 2 * (ks & 1) + h;
 }
 
@@ -115,6 +123,9 @@ __device__ __forceinline__ int d_to_kpos(int d)
     } else if constexpr (KC == KVQ_CODEC_Q4_G32) {
         const int g = d >> 5, t = (d & 31) >> 3, w = d & 7, h = w >> 2, sub = (w >> 1) & 1, hi = w & 1;
         return 16 * (2 * g + sub) + 8 * hi + 2 * t + h;
+    } else if constexpr (KC == KVQ_CODEC_NVFP4) {
+        const int g = d >> 6, r = d & 63, hi = r >> 5, t = (r & 31) >> 3, k = (r & 7) >> 1, h = r & 1;
+        return 16 * (4 * g + k) + 8 * hi + 2 * t + h;
     } else {
         const int g = d >> 5, r = d & 31, hi = r >> 4, t = (r & 15) >> 2, st = (r >> 1) & 1, h = r & 1;
         return 16 * (2 * g + st) + 8 * hi + 2 * t + h;
@@ -170,6 +181,41 @@ __device__ __forceinline__ void q8_pairs(uint32_t w, uint32_t &ev, uint32_t &od)
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(od) : "r"(o), "r"(0x64806480u));
 }
 
+// NVFP4 K after ldmatrix: the 4 bytes of a word hold head_dim values
+// (2e, 2e + 1) of one token in byte e; each becomes an fp16x2 by the hardware
+// E2M1 conversion, multiplied (exactly) by the block's scale pair.
+__device__ __forceinline__ uint32_t fp4_byte_h2(uint32_t w, int e, uint32_t s2)
+{
+    const uint32_t h = e2m1x2_to_h2(w >> (8 * e));
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(s2));
+    return r;
+}
+
+// An E4M3 byte (bits 0-7 of b) as the fp16x2 pair (s, s).
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t b)
+{
+    uint32_t d, h2;
+    asm("prmt.b32 %0, %1, 0, 0x0000;" : "=r"(d) : "r"(b));
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(d));
+    return h2;
+}
+
+// NVFP4 V after ldmatrix.trans: a word holds nibbles e = 0..3 (head_dim
+// values 4 gid + e) of token t0 in bits 0-15 and of t1 in bits 16-31; pair e
+// gathers nibble e of both into one byte (0xE4 = (a & c) | (b & ~c)), the
+// hardware E2M1 conversion makes it (t0, t1) as fp16x2, times the tokens'
+// scales s2.
+__device__ __forceinline__ uint32_t fp4_pair(uint32_t w, int e, uint32_t s2)
+{
+    const uint32_t lo = w >> (4 * e), hi = w >> (12 + 4 * e);
+    uint32_t b, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(b) : "r"(lo), "r"(hi), "r"(0x0000000Fu));
+    const uint32_t h = e2m1x2_to_h2(b);
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(s2));
+    return r;
+}
+
 // The pair without any offset: q for even e, 16 q for odd e (an exact fp16
 // subtraction of 1032 = 0x6408 or 1152 = 0x6480 from the biased form).
 __device__ __forceinline__ uint32_t q4_pair(uint32_t w, int e)
@@ -192,7 +238,7 @@ template <int KC, int D, int ROWS, typename QT>
 __device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb_s, int R, bool ok)
 {
     constexpr int CPR = D / 8;                     // chunks per row
-    constexpr int CPG = group_size(KC) / 8;        // chunks per K group
+    constexpr int CPG = (is_fp4(KC) ? 64 : group_size(KC)) / 8;   // chunks per K accumulation group
     for (int ci = threadIdx.x; ci < ROWS * CPR; ci += kT) {    // whole warps per step
         const int n = ci / CPR, c = ci % CPR;
         float x[8];
@@ -217,7 +263,7 @@ __device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb
             // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
             const int kg = 8 * c + 2 * j;
             const bool even = is_q4(KC) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
-            b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
+            if constexpr (!is_fp4(KC)) b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
         }
         *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
 #pragma unroll
@@ -254,7 +300,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     using KG = TileGeom<C::KRB>;
     using VG = TileGeom<C::VRB>;
     constexpr int NGK = C::NGK;
-    constexpr int KSTEP_PER_G = group_size(KC) / 16;
+    constexpr int KSTEP_PER_G = C::KGS / 16;
     constexpr int MTW = C::MTW;
 
     extern __shared__ uint8_t smem_raw[];
@@ -369,10 +415,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     // values), rows 0-7 its even, rows 8-15 its odd head_dim indices; one
     // ldmatrix.x4.trans covers two chunks.
     constexpr bool V8 = (VC == KVQ_CODEC_Q8_0);
+    constexpr bool F4V = is_fp4(VC);        // NVFP4 V: Q4's tile layout, exact scaled values
     const int cw = (warp * MTW) >> 1, cw1 = (MTW == 4) ? cw + 1 : cw;
-    constexpr int NGW = (MTW == 4 && VC != KVQ_CODEC_Q4_G64) ? 2 : 1;    // V groups a warp's tiles touch
+    constexpr int NGW = (MTW == 4 && VC != KVQ_CODEC_Q4_G64 && !F4V) ? 2 : 1;  // V groups a warp's tiles touch
     // V codes as fp16 subnormals with their offset removed per tile (one n-tile)
-    constexpr bool kSubV = (NT == 1 && (NGW == 1 || V8));
+    constexpr bool kSubV = (NT == 1 && (NGW == 1 || V8)) && !F4V;
     const int gv0 = V8 ? (MTW * warp) / 2 : (32 * cw) / group_size(VC);  // the first of them
     constexpr int NLV = V8 ? (MTW + 1) / 2 : 1;                          // ldmatrix per 16 tokens
     uint32_t voff[NLV];
@@ -416,22 +463,46 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         __half *vt = vt0 + (jj & 1) * (C::NGV * kTile);
         for (int i = lane; i < 16 * C::NGV; i += 32) {
             const int t = i & 15, g = i >> 4;
-            vt[g * kTile + tl + t] =
-                (tb + t < hi) ? reinterpret_cast<const __half *>(vsp + (tl + t) * C::VSB)[g] : __float2half_rn(0.0f);
+            __half sv = __float2half_rn(0.0f);
+            if (tb + t < hi) {
+                if constexpr (is_fp4(VC)) sv = __float2half_rn(e4m3_to_float(vsp[(tl + t) * C::VSB + g]));
+                else sv = reinterpret_cast<const __half *>(vsp + (tl + t) * C::VSB)[g];
+            }
+            vt[g * kTile + tl + t] = sv;
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) sc[nt][c] = 0.0f;
         float sk0[NGK], sk1[NGK];
-        load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
-        load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
+        if constexpr (is_fp4(KC)) {
+#pragma unroll
+            for (int g = 0; g < NGK; ++g) sk0[g] = sk1[g] = 1.0f;     // the scales go into the operands
+        } else {
+            load_scales<NGK>(ksp + (tl + gid) * C::KSB, sk0);
+            load_scales<NGK>(ksp + (tl + gid + 8) * C::KSB, sk1);
+        }
 #pragma unroll
         for (int u = 0; u < NLU; ++u) {
             uint32_t r0, r1, r2, r3;
             ldsm_x4(base + koff[u], r0, r1, r2, r3);
             uint32_t h0[4], h1[4], h2[4], h3[4];
-            if constexpr (is_q4(KC)) {
+            if constexpr (is_fp4(KC)) {
+                // this lane's 8 values of a chunk are one 16-value block: block
+                // 4u + tig / 2 (chunk 2u) and 4u + 2 + tig / 2 (chunk 2u + 1)
+                const int ba = 4 * u + (tig >> 1), bb = ba + 2;
+                const uint32_t s0a = e4m3_pair(ksp[(tl + gid) * C::KSB + ba]);
+                const uint32_t s1a = e4m3_pair(ksp[(tl + gid + 8) * C::KSB + ba]);
+                const uint32_t s0b = e4m3_pair(ksp[(tl + gid) * C::KSB + bb]);
+                const uint32_t s1b = e4m3_pair(ksp[(tl + gid + 8) * C::KSB + bb]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    h0[e] = fp4_byte_h2(r0, e, s0a);
+                    h1[e] = fp4_byte_h2(r1, e, s1a);
+                    h2[e] = fp4_byte_h2(r2, e, s0b);
+                    h3[e] = fp4_byte_h2(r3, e, s1b);
+                }
+            } else if constexpr (is_q4(KC)) {
                 unpack_q4_biased(r0, h0);
                 unpack_q4_biased(r1, h1);
                 unpack_q4_biased(r2, h2);
@@ -614,9 +685,17 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 lg[nt] += (p[nt][0] + p[nt][1]) + (p[nt][2] + p[nt][3]);
             }
             // P' = p * v_scale(token, group), one B fragment set per V group
+            // (NVFP4: P' = p, the scales are in the V operands)
             uint32_t b0[NGW][NT], b1[NGW][NT];
+            if constexpr (F4V) {
 #pragma unroll
-            for (int q = 0; q < NGW; ++q) {
+                for (int nt = 0; nt < NT; ++nt) {
+                    b0[0][nt] = pack_f16x2(p[nt][0], p[nt][1]);
+                    b1[0][nt] = pack_f16x2(p[nt][2], p[nt][3]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < NGW && !F4V; ++q) {
                 const __half *vq = vt + (gv0 + q) * kTile + 16 * kk + 2 * tig;
                 const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(vq));
                 const float2 s89 = __half22float2(*reinterpret_cast<const __half2 *>(vq + 8));
@@ -650,7 +729,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                 const int lc = (MTW >= 2) ? (t >> 1) : 0;
                 const int j = (MTW >= 2) ? (t & 1) : (warp & 1);
                 const uint32_t ra = lc ? rv[0][1] : rv[0][0], rb = lc ? rv[0][3] : rv[0][2];
-                if constexpr (kSubV) {
+                if constexpr (F4V) {
+                    // the lane's head_dim values 32 c + 4 gid + e lie in block 2 c + gid / 4;
+                    // the scales of tokens (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9)
+                    const __half *vq = vt + (2 * (cw + lc) + (gid >> 2)) * kTile + 16 * kk + 2 * tig;
+                    const uint32_t s01 = *reinterpret_cast<const uint32_t *>(vq);
+                    const uint32_t s89 = *reinterpret_cast<const uint32_t *>(vq + 8);
+                    a0 = fp4_pair(ra, 2 * j, s01); a1 = fp4_pair(ra, 2 * j + 1, s01);
+                    a2 = fp4_pair(rb, 2 * j, s89); a3 = fp4_pair(rb, 2 * j + 1, s89);
+                } else if constexpr (kSubV) {
                     a0 = q4_pair_sub(ra, 2 * j); a1 = q4_pair_sub(ra, 2 * j + 1);
                     a2 = q4_pair_sub(rb, 2 * j); a3 = q4_pair_sub(rb, 2 * j + 1);
                 } else {
@@ -762,7 +849,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             // the V codes entered as q 2^-24 or q (even head_dim index) and, for the
             // 4-bit codecs, 16 times that (odd)
             const float inv = empty ? 0.0f : (kSubV ? 0x1p24f : 1.0f) / L;
-            const float inv16 = V8 ? inv : inv * 0.0625f;
+            const float inv16 = (V8 || F4V) ? inv : inv * 0.0625f;
             const int i = n / G, jj = n % G;
             const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
             float *dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
@@ -905,6 +992,7 @@ cudaError_t launch_k(const DecodeArgs &a, cudaStream_t st)
     case KVQ_CODEC_Q4_G64: return launch_d<KVQ_CODEC_Q4_G64, VC, QT>(a, st);
     case KVQ_CODEC_Q8_0: return launch_d<KVQ_CODEC_Q8_0, VC, QT>(a, st);
     case KVQ_CODEC_Q4_G32: return launch_d<KVQ_CODEC_Q4_G32, VC, QT>(a, st);
+    case KVQ_CODEC_NVFP4: return launch_d<KVQ_CODEC_NVFP4, VC, QT>(a, st);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -923,6 +1011,7 @@ int per_sm_for_v(int k_codec, int head_dim, int nt)
     case KVQ_CODEC_Q4_G64: return per_sm_d<KVQ_CODEC_Q4_G64, VC>(head_dim, nt);
     case KVQ_CODEC_Q8_0: return per_sm_d<KVQ_CODEC_Q8_0, VC>(head_dim, nt);
     case KVQ_CODEC_Q4_G32: return per_sm_d<KVQ_CODEC_Q4_G32, VC>(head_dim, nt);
+    case KVQ_CODEC_NVFP4: return per_sm_d<KVQ_CODEC_NVFP4, VC>(head_dim, nt);
     default: return 0;
     }
 }

@@ -132,11 +132,13 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // CTAs of the tensor-core decode kernel that fit on one SM for these caches and
 // query rows per kv head; 0 if that kernel does not take them or no device answers.
 int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_head);
-// The same kernel for V in Q4_G32 and in q8_0 (translation units of their own).
+// The same kernel for V in Q4_G32, q8_0 and NVFP4 (translation units of their own).
 cudaError_t launch_decode_tc_g32(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 int decode_tc_g32_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 cudaError_t launch_decode_tc_q8v(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 int decode_tc_q8v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
+cudaError_t launch_decode_tc_fp4v(const DecodeArgs &a, int q_dtype, cudaStream_t st);
+int decode_tc_fp4v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int rows, int head_dim,
                          float *out, float *out_lse, cudaStream_t st);
 cudaError_t launch_dequant(const Plane &p, int64_t n_rows, int head_dim, float *out, cudaStream_t st);

@@ -75,8 +75,8 @@ def test_codec_pairs(kc, vc, D):
         check_close(o, o_ref, lse, lse_ref)
 
 
-@pytest.mark.parametrize("kc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32])
-@pytest.mark.parametrize("vc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0])
+@pytest.mark.parametrize("kc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_NVFP4])
+@pytest.mark.parametrize("vc", [kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_NVFP4])
 @pytest.mark.parametrize("G,n_new", [(1, 1), (6, 3), (8, 4)])
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
