@@ -207,7 +207,8 @@ def run_reference(args, wl, kv_bytes):
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-_CODEC_NAME = {workloads.Q4_G64: "q4_g64", workloads.Q8_0: "q8_0", workloads.Q4_G32: "q4_g32"}
+_CODEC_NAME = {workloads.Q4_G64: "q4_g64", workloads.Q8_0: "q8_0", workloads.Q4_G32: "q4_g32",
+               workloads.NVFP4: "nvfp4"}
 
 
 def _config(wl, args, extra=None):

@@ -31,6 +31,8 @@ V bias, the outlier mask and the sequence lengths):
   5 ship65k   as 2 with K q8_0 / V Q4_G32 (the pages' shipped -ctk q8_0 -ctv q4_0
               pair, q4_0 read as Q4 with 32-value groups); not a benchmark
               workload, it carries that pair through the same tests.
+  6 nvfp4_65k as 2 with K and V in NVFP4 (the pages' matched -ctk nvfp4 -ctv
+              nvfp4 KV type); likewise a test case.
 """
 from __future__ import annotations
 
@@ -89,10 +91,12 @@ def spec(index: int) -> Spec:
                     len_range=(1024, 65536))
     if index == 5:
         return Spec("ship65k", 1, 24, 4, 256, (65535,), 1, Q8_0, Q4_G32, "f16", "f16", "normal", s)
+    if index == 6:
+        return Spec("nvfp4_65k", 1, 24, 4, 256, (65535,), 1, NVFP4, NVFP4, "f16", "f16", "normal", s)
     raise ValueError(index)
 
 
-N_CONFIGS = 6                # 0..4 the benchmark's workloads, 5 the shipped q8_0-K / q4_0-V pair
+N_CONFIGS = 7                # 0..4 the benchmark's workloads, 5 the shipped q8_0-K / q4_0-V pair, 6 NVFP4
 
 
 @dataclasses.dataclass
