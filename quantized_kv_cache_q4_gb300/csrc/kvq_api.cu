@@ -84,7 +84,9 @@ int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int3
                    int32_t n_splits)
 {
     if (n_splits > 0) return n_splits;
-    const int64_t units = (int64_t)k->n_seq * k->n_kv_heads;
+    // one CTA per (sequence, kv head, block of query rows) and split
+    const int rows = n_q * (n_heads / k->n_kv_heads);
+    const int64_t units = (int64_t)k->n_seq * k->n_kv_heads * (k->head_dim <= 256 ? kvq::tc_row_blocks(rows) : 1);
     int64_t target;
     if (k->n_seq == 1) {
         // one wave of the decode kernel's CTAs

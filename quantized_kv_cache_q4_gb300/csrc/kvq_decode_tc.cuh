@@ -315,12 +315,15 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     __shared__ volatile int s_timeout;
     __shared__ int s_issued;
 
-    const int split = blockIdx.x, kh = blockIdx.y;
+    // grid y: kv head x block of up to 8 NT query rows (one block unless a kv
+    // head has more than 32 rows, as a prompt chunk does)
+    const int split = blockIdx.x, kh = blockIdx.y / a.n_row_blocks, rblk = blockIdx.y % a.n_row_blocks;
     __shared__ int s_seq;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int G = a.n_heads / a.n_kv_heads;
-    const int R = a.n_q * G;                             // <= 8 * NT
+    const int r0 = rblk * 8 * NT;                         // this CTA's first row of the kv head
+    const int R = min(8 * NT, a.n_q * G - r0);           // its rows
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
@@ -349,24 +352,37 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         __syncthreads();
         s = s_seq;
     }
-    // query rows (for each query token, the G heads of this kv head are one
-    // contiguous run) by bulk copy, in parallel with what follows
+    // query rows r0 .. r0 + R - 1 (row r is head r % G of query token r / G;
+    // a token's heads of this kv head are one contiguous run) by bulk copy, in
+    // parallel with what follows
     if (threadIdx.x == 0) {
-        const uint32_t run = (uint32_t)(G * D * sizeof(QT));
-        mbar_expect_tx(bar_q, run * (uint32_t)a.n_q);
+        const uint32_t row = (uint32_t)(D * sizeof(QT));
+        mbar_expect_tx(bar_q, row * (uint32_t)R);
         const QT *q = static_cast<const QT *>(a.q);
-        for (int i = 0; i < a.n_q; ++i)
-            bulk_load(smem_u32(smem + C::QST_OFF) + i * run, q + (((int64_t)s * a.n_q + i) * a.n_heads + kh * G) * D,
-                      run, bar_q);
+        if (a.n_row_blocks == 1) {           // all n_q tokens, G heads each (no division on this path)
+            for (int i = 0; i < a.n_q; ++i)
+                bulk_load(smem_u32(smem + C::QST_OFF) + (uint32_t)(i * G) * row,
+                          q + (((int64_t)s * a.n_q + i) * a.n_heads + kh * G) * D, (uint32_t)G * row, bar_q);
+        } else {
+            for (int i = r0 / G; i <= (r0 + R - 1) / G; ++i) {
+                const int j0 = max(0, r0 - i * G), j1 = min(G, r0 + R - i * G);
+                bulk_load(smem_u32(smem + C::QST_OFF) + (uint32_t)(i * G + j0 - r0) * row,
+                          q + (((int64_t)s * a.n_q + i) * a.n_heads + kh * G + j0) * D, (uint32_t)(j1 - j0) * row,
+                          bar_q);
+            }
+        }
     }
 
     int len = a.kv_len[s];
     if (len < 0 || len > a.max_kv_len) {
-        if (threadIdx.x == 0 && split == 0 && kh == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
+        if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
         len = len < 0 ? 0 : a.max_kv_len;
     }
     int lo, hi;
     split_range(len, a.n_splits, split, lo, hi);
+    // no row of this CTA sees past its last query token's keys (with one row
+    // block the last row is the last query token, which sees them all)
+    if (a.n_row_blocks > 1) hi = max(lo, min(hi, len - a.n_q + (r0 + R - 1) / G + 1));
     const int n_tiles = (int)ceil_div(hi - lo, kTile);
     const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
     const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
@@ -391,7 +407,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int r = nt * 8 + 2 * tig + c;
-            nv[nt][c] = r < R ? len - a.n_q + r / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
+            nv[nt][c] = r < R ? len - a.n_q + (r0 + r) / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
             nv_min = min(nv_min, nv[nt][c]);
         }
     const float sl2 = a.scale_log2;
@@ -850,7 +866,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
             // 4-bit codecs, 16 times that (odd)
             const float inv = empty ? 0.0f : (kSubV ? 0x1p24f : 1.0f) / L;
             const float inv16 = (V8 || F4V) ? inv : inv * 0.0625f;
-            const int i = n / G, jj = n % G;
+            const int i = (r0 + n) / G, jj = (r0 + n) % G;
             const int64_t orow = ((int64_t)s * a.n_q + i) * a.n_heads + kh * G + jj;
             float *dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
             if constexpr (V8) {
@@ -921,7 +937,7 @@ cudaError_t launch_cfg(Kern kern, const DecodeArgs &a, cudaStream_t st)
     int per_sm = 0;
     cudaError_t e = prepare_kernel<C>(kern, &per_sm);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
+    dim3 grid(a.n_splits, a.n_kv_heads * a.n_row_blocks, a.n_seq);
     return launch_pdl(kern, grid, dim3(kT), C::SMEM, st, a, tk, tv);
 }
 
@@ -965,7 +981,7 @@ template <int KC, int VC, int D, typename QT>
 cudaError_t launch_nt(const DecodeArgs &a, cudaStream_t st)
 {
     const int R = a.n_q * (a.n_heads / a.n_kv_heads);
-    switch ((R + 7) / 8) {
+    switch (R > 32 ? 4 : (R + 7) / 8) {
     case 1: return launch_t<KC, VC, D, 1, QT>(a, st);
     case 2: return launch_t<KC, VC, D, 2, QT>(a, st);
     case 3: return launch_t<KC, VC, D, 3, QT>(a, st);

@@ -108,7 +108,16 @@ struct DecodeArgs {
     float *out, *out_lse;       // final results (used when n_splits == 1)
     float *part_o, *part_lse;   // [n_splits][rows][D], [n_splits][rows] (n_splits > 1)
     int32_t *err;
+    int n_row_blocks = 1;       // tensor-core kernel: CTAs per (split, kv head), 32 query rows each
 };
+
+// Query rows per kv head the tensor-core kernel gives one CTA, and the blocks
+// of them a kv head with R rows takes.
+constexpr int kTcRowsPerCta = 32;
+inline int tc_row_blocks(int rows_per_kv_head)
+{
+    return rows_per_kv_head > kTcRowsPerCta ? (int)ceil_div(rows_per_kv_head, kTcRowsPerCta) : 1;
+}
 
 // Token range [lo, hi) of split `split` for a sequence whose last query row
 // sees `len` keys: chunks of ceil(len / n_splits) rounded up to 64 tokens.
@@ -126,7 +135,8 @@ void set_last_error(const char *msg);
 
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);
-// Tensor-core path: 1..32 query rows per kv head, head_dim 64/128/256, any K and V codec.
+// Tensor-core path: head_dim 64/128/256, any K and V codec, any number of query
+// rows per kv head (blocks of up to 32 rows, one CTA each).
 bool decode_tc_supported(const DecodeArgs &a);
 cudaError_t launch_decode_tc(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // CTAs of the tensor-core decode kernel that fit on one SM for these caches and

@@ -127,6 +127,25 @@ def test_nvfp4_pairs(kc, vc, G, n_new, D):
         check_close(o, o_ref, lse, lse_ref)
 
 
+@pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G64),
+                                   (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4)])
+@pytest.mark.parametrize("D", [128, 256, 512])
+@pytest.mark.parametrize("n_new", [40, 7])
+def test_prompt_chunk(kc, vc, D, n_new):
+    """A chunk of new prompt tokens attending causally to the cache and to each
+    other (chunked prefill): 6 query heads per kv head x 40 (or 7) tokens = 240
+    (42) rows per kv head, blocks of 32 rows on the tensor cores (head_dim <=
+    256) with a ragged last block; rows of early tokens see fewer keys."""
+    wl = workloads.custom(n_seq=2, n_heads=12, n_kv_heads=2, head_dim=D, cached=(1000 - n_new, 150), n_new=n_new,
+                          k_codec=kc, v_codec=vc, src_dtype="f16", q_dtype="f16", seed=kc + 3 * vc + D + n_new)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (0, 1, 4):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
 def test_rows_without_keys():
     """kv_len < n_q: the first rows see no key -> out = 0, lse = -inf."""
     wl = workloads.custom(n_seq=2, n_heads=6, n_kv_heads=1, head_dim=128, cached=(0, 10), n_new=3, src_dtype="f16",
