@@ -1,6 +1,7 @@
 // kvq_decode_tc.cuh -- split-K decode / MTP-verify attention over a packed cache
-// on the tensor cores, for 1..32 query rows per kv head (GQA group x query
-// tokens), head_dim 64/128/256, K and V each in Q4_G64, Q4_G32, q8_0 or
+// on the tensor cores, for any number of query rows per kv head (GQA group x
+// query tokens; up to 32 in one CTA, more -- a prompt chunk -- in blocks of
+// 32, one CTA each), head_dim 64/128/256, K and V each in Q4_G64, Q4_G32, q8_0 or
 // NVFP4 (the kernel template; kvq_decode_tc.cu, kvq_decode_tc_g32.cu,
 // kvq_decode_tc_q8v.cu and kvq_decode_tc_fp4v.cu hold its instances for the
 // four V codecs, so that they compile in parallel).  NVFP4 codes enter the
