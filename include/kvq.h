@@ -153,10 +153,10 @@ int32_t kvq_decode_default_splits(const kvq_cache *k, const kvq_cache *v, int32_
 size_t kvq_decode_workspace_bytes(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
                                   int32_t max_kv_len, int32_t n_splits);
 
-/* Decode / MTP-verify attention over the packed cache (the attention stage).
- *   k, v          : caches with the same n_seq, n_kv_heads, head_dim, capacity.
- *                   Supported pairs: (Q4_G64, Q4_G64), (Q8_0, Q4_G64), (Q4_G64, Q8_0),
- *                   (Q8_0, Q8_0).
+/* Decode / MTP-verify attention over the packed cache (the attention stage);
+ * with n_q new prompt tokens it is the attention of a chunked prefill.
+ *   k, v          : caches with the same n_seq, n_kv_heads, head_dim, capacity;
+ *                   any pair of codecs.
  *   q             : DEVICE, [n_seq][n_q][n_heads][head_dim], dtype q_dtype, 16-byte aligned.
  *                   Query head h reads kv head h / (n_heads / n_kv_heads).
  *   softmax_scale : multiplies q.k (e.g. 1/sqrt(head_dim)).
@@ -177,8 +177,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache *k, const kvq_cache *v, int32_
  *                   256-byte aligned; may be NULL when that size is 0.  Its
  *                   contents need no initialisation and are not kept.
  *   d_err         : DEVICE int32, nullable (KVQ_ERR_KV_LEN, KVQ_ERR_TIMEOUT).
- * Arithmetic: codes are exact in fp16, dot products accumulate in fp32 and the
- * softmax runs in fp32. */
+ * Arithmetic: codes (NVFP4: code values times their E4M3 scales) are exact in
+ * fp16, dot products accumulate in fp32 and the softmax runs in fp32; the
+ * softmax weights enter the weighted sum of V rounded to fp16. */
 kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v,
                                 const void *q, int32_t q_dtype, int32_t n_q, int32_t n_heads,
                                 float softmax_scale, const int32_t *d_kv_len, int32_t max_kv_len,

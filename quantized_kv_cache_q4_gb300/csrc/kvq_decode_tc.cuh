@@ -18,8 +18,8 @@
 //
 // Work of one CTA (four warps, no dedicated producer), one CTA barrier per tile:
 //  * Thread 0 fetches the query rows with 1D bulk copies and the first tiles of
-//    64 tokens (K and V codes by swizzled 2D TMA, their fp16 scales by bulk
-//    copies) into a 3-stage shared-memory ring.  After the barrier of tile j it
+//    64 tokens (K and V codes by swizzled 2D TMA, their scales by bulk
+//    copies) into a 3-stage (2 for q8_0 K and V) shared-memory ring.  After the barrier of tile j it
 //    refills the stage of tile j - 1, which every warp has finished with.
 //  * Phase A: warp w computes S^T = K Q^T for tokens [16w, 16w+16) of the tile
 //    and all n-tiles of 8 rows on mma.sync.m16n8k16.  The K codes enter as
@@ -414,7 +414,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     const float sl2 = a.scale_log2;
     const int tl = warp * 16;                                           // phase A tokens
     // K fragments: one ldmatrix.x4 per 32 bytes of a token row (two 16-byte
-    // chunks: one group of Q4_G64 or q8_0, two groups of Q4_G32)
+    // chunks: one group of Q4_G64 or q8_0, two groups of Q4_G32, four NVFP4 blocks)
     constexpr int NLU = C::KRB / 32;
     constexpr int GPU = (KC == KVQ_CODEC_Q4_G32) ? 2 : 1;          // K groups per ldmatrix
     uint32_t koff[NLU];
