@@ -104,6 +104,11 @@ int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int3
     const int64_t max_useful = kvq::ceil_div(max_kv_len, 256);      // at least 256 tokens a split
     if (s > max_useful) s = max_useful;
     if (s < 1) s = 1;
+    // splits are whole 64-token tiles (split_range): with t tiles and s splits
+    // of ceil(t / s) tiles each, only ceil(t / ceil(t / s)) of them get any;
+    // ask for exactly those (the same longest split, no empty ones)
+    const int64_t tiles = kvq::ceil_div(max_kv_len, 64);
+    if (tiles > 0) s = kvq::ceil_div(tiles, kvq::ceil_div(tiles, s));
     if (s > kMaxSplits) s = kMaxSplits;
     return (int)s;
 }
