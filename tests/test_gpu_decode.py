@@ -48,7 +48,7 @@ def test_small_sweep(L, n_new, G, D):
         check_close(o, o_ref, lse, lse_ref)
 
 
-@pytest.mark.parametrize("n_splits", [1, 2, 7, 64, 256])
+@pytest.mark.parametrize("n_splits", [1, 2, 7, 8, 16, 64, 256])
 def test_split_counts(n_splits):
     wl = workloads.custom(n_seq=2, n_heads=12, n_kv_heads=2, head_dim=256, cached=(5000, 1234), n_new=3,
                           src_dtype="f16", q_dtype="f16", dist="outliers", seed=40)
