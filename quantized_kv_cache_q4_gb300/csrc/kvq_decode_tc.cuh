@@ -100,8 +100,8 @@ struct TcCfg {
 };
 
 // head_dim index fed by k-position kp (0..15) of k-step ks, in the order the K
-// unpack delivers values (Q4_G64: pairs (d, d + 4) of a 4-byte piece; q8_0:
-// pairs (d, d + 1)), and its inverse.
+// unpack delivers values (Q4_G64: pairs (d, d + 4) of a 4-byte piece; q8_0 and
+// NVFP4: pairs (d, d + 1)).
 template <int KC>
 __device__ __forceinline__ int kpos_to_d(int ks, int kp)
 {
@@ -115,23 +115,6 @@ __device__ __forceinline__ int kpos_to_d(int ks, int kp)
     else return 32 * (ks >> 1) + 16 * hi + 4 * t + 2 * (ks & 1) + h;
 }
 
-template <int KC>
-__device__ __forceinline__ int d_to_kpos(int d)
-{
-    if constexpr (KC == KVQ_CODEC_Q4_G64) {
-        const int g = d >> 6, r = d & 63, hi = r >> 5, t = (r & 31) >> 3, st = r & 3, h = (r >> 2) & 1;
-        return 16 * (4 * g + st) + 8 * hi + 2 * t + h;
-    } else if constexpr (KC == KVQ_CODEC_Q4_G32) {
-        const int g = d >> 5, t = (d & 31) >> 3, w = d & 7, h = w >> 2, sub = (w >> 1) & 1, hi = w & 1;
-        return 16 * (2 * g + sub) + 8 * hi + 2 * t + h;
-    } else if constexpr (KC == KVQ_CODEC_NVFP4) {
-        const int g = d >> 6, r = d & 63, hi = r >> 5, t = (r & 31) >> 3, k = (r & 7) >> 1, h = r & 1;
-        return 16 * (4 * g + k) + 8 * hi + 2 * t + h;
-    } else {
-        const int g = d >> 5, r = d & 31, hi = r >> 4, t = (r & 15) >> 2, st = (r >> 1) & 1, h = r & 1;
-        return 16 * (2 * g + st) + 8 * hi + 2 * t + h;
-    }
-}
 
 // byte offset of 16-byte chunk c of row n of the permuted query copy (D halves a row)
 template <int D>

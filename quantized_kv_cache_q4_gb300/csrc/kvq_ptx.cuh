@@ -1,6 +1,6 @@
 // kvq_ptx.cuh -- inline-PTX building blocks of the tensor-core decode kernels:
 // mbarriers with bounded waits, TMA (2D tiled and 1D bulk) loads, ldmatrix /
-// movmatrix / mma.sync, the signed-nibble and int8 unpack to exact fp16
+// mma.sync, the signed-nibble and int8 unpack to exact fp16
 // integers, the swizzled tile geometry and the tensor-map encoder.
 #pragma once
 
@@ -29,10 +29,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
@@ -112,12 +108,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "r"(addr));
 }
 
-__device__ __forceinline__ uint32_t movm_t(uint32_t a)
-{
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
@@ -160,39 +150,10 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_c
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 // Eight signed 4-bit codes of a 32-bit word (nibble p = bits 4p..4p+3) as four
-// fp16x2 integers: h[0] = (p0, p4), h[1] = (p1, p5), h[2] = (p2, p6), h[3] = (p3, p7).
-// A nibble n becomes the fp16 1024 + (n ^ 8) (or 1024 + 16 (n ^ 8) for the odd
-// positions); subtracting 1032 (or scaling by 1/16 and subtracting 72) leaves
-// the two's complement value exactly.
-__device__ __forceinline__ void unpack_q4(uint32_t w, uint32_t (&h)[4])
-{
-    const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));   // 1032
-    const __half2 k16th = __half2half2(__ushort_as_half(0x2C00));   // 1/16
-    const __half2 km72 = __half2half2(__ushort_as_half(0xD480));    // -72
-    const uint32_t w8 = w >> 8;
-    h[0] = h2_as_u32(__hsub2(u32_as_h2(lop3_ac(w, 0x64086408u, 0x64076407u)), k1032));
-    h[1] = h2_as_u32(__hfma2(u32_as_h2(lop3_ac(w, 0x64806480u, 0x64706470u)), k16th, km72));
-    h[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_ac(w8, 0x64086408u, 0x64076407u)), k1032));
-    h[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_ac(w8, 0x64806480u, 0x64706470u)), k16th, km72));
-}
-
-// Four signed 8-bit codes (byte j = value j) as two fp16x2 integers (b0, b1), (b2, b3):
-// byte b becomes 0x64 : (b ^ 0x80) = 1024 + b + 128, minus 1152.
-__device__ __forceinline__ void unpack_q8(uint32_t w, uint32_t (&h)[2])
-{
-    const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));   // 1152
-    const uint32_t x = w ^ 0x80808080u;
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x7342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
-    h[0] = h2_as_u32(__hsub2(u32_as_h2(a), k1152));
-    h[1] = h2_as_u32(__hsub2(u32_as_h2(b), k1152));
-}
-
-// The same codes with their fp16 bias left in, for operands whose bias is
-// removed after the MMA: h[0], h[2] = 1032 + q (nibble positions 0,4 and 2,6,
-// the even head_dim indices), h[1], h[3] = 1152 + 16 q (the odd indices).
-// One LOP3 per two values.
+// fp16x2 integers with their bias left in, for operands whose bias is removed
+// after the MMA: h[0] = (p0, p4), h[2] = (p2, p6) as 1032 + q (the even
+// head_dim indices), h[1] = (p1, p5), h[3] = (p3, p7) as 1152 + 16 q (the odd
+// ones).  One LOP3 per two values.
 __device__ __forceinline__ void unpack_q4_biased(uint32_t w, uint32_t (&h)[4])
 {
     const uint32_t w8 = w >> 8;
