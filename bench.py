@@ -58,13 +58,18 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# The sources of the kernels the committed captures profile (the Q4_G64 decode
+# and the merge) and of their launch (split policy, tensor maps).
+_PROFILED_SOURCES = ("kvq_api.cu", "kvq_decode_tc.cu", "kvq_decode_tc.cuh", "kvq_internal.cuh", "kvq_merge.cu",
+                     "kvq_ptx.cuh", "kvq_tensor_map.cu")
+
+
 def _kernel_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_kv_cache_q4_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in _PROFILED_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 

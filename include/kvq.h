@@ -119,6 +119,13 @@ int32_t kvq_scales_per_row(int32_t codec, int32_t head_dim);
 /* Bytes of one scale (2: fp16; 1: E4M3 for NVFP4), or 0 for an unknown codec. */
 int32_t kvq_scale_bytes(int32_t codec);
 
+/* Failure-path self-test: enqueues one CTA that waits, with the bounded device
+ * wait every kernel of the library uses for its copies, on a barrier nothing
+ * completes.  After the wait's cycle limit (about 1 s) it ORs
+ * KVQ_ERR_TIMEOUT into *d_err (DEVICE int32) and returns; nothing traps and
+ * the context stays usable.  KVQ_EINVAL if d_err is NULL. */
+kvq_status kvq_selftest_bounded_wait(int32_t *d_err, void *stream);
+
 /* Quantize-on-append (the KV-cache append stage).
  *   k_src, v_src : DEVICE, [n_seq][n_new][n_kv_heads][head_dim], dtype src_dtype
  *                  (KVQ_F32 or KVQ_F16), 16-byte aligned.

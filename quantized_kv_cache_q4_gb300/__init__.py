@@ -50,6 +50,7 @@ def _load():
         "kvq_row_bytes": (I32, [I32, I32]),
         "kvq_scales_per_row": (I32, [I32, I32]),
         "kvq_scale_bytes": (I32, [I32]),
+        "kvq_selftest_bounded_wait": (I32, [P, P]),
         "kvq_quantize_append": (I32, [C, C, P, P, I32, I32, P, P, P]),
         "kvq_decode_default_splits": (I32, [C, C, I32, I32, I32]),
         "kvq_decode_workspace_bytes": (SZ, [C, C, I32, I32, I32, I32]),
@@ -70,7 +71,8 @@ def _load():
 _lib = _load()
 EXPORTED = ("kvq_row_bytes", "kvq_scales_per_row", "kvq_scale_bytes", "kvq_quantize_append", "kvq_decode_default_splits",
             "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_merge_splits", "kvq_dequantize",
-            "kvq_status_string", "kvq_last_error", "kvq_static_scratch_bytes", "kvq_decode_attention_static")
+            "kvq_status_string", "kvq_last_error", "kvq_static_scratch_bytes", "kvq_decode_attention_static",
+            "kvq_selftest_bounded_wait")
 
 
 def _check(status: int):
@@ -104,6 +106,12 @@ def kvq_scales_per_row(codec: int, head_dim: int) -> int:
 
 def kvq_scale_bytes(codec: int) -> int:
     return int(_lib.kvq_scale_bytes(codec))
+
+
+def kvq_selftest_bounded_wait(d_err, stream=None):
+    """Run the library's bounded device wait on a barrier nothing completes: after
+    about 1 s KVQ_ERR_TIMEOUT is OR-ed into d_err (see include/kvq.h)."""
+    _check(_lib.kvq_selftest_bounded_wait(_ptr(d_err), _stream(stream)))
 
 
 class KVCache:
