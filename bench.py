@@ -54,7 +54,7 @@ def _peaks():
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
-    except Exception:
+    except (OSError, ValueError, KeyError, TypeError):      # no file, not JSON, no or bad entry
         return 6800.0, "fallback"
 
 
@@ -82,7 +82,7 @@ def _traffic(config_name: str):
         e = t.get(config_name)
         if e and e.get("kernel_hash") == _kernel_hash():
             return e["dram_bytes_per_launch"]
-    except Exception:
+    except (OSError, ValueError, KeyError):                  # no capture recorded for these sources
         pass
     return None
 
@@ -104,7 +104,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
-        except Exception:
+        except OSError:                                       # no nvidia-smi: no clock record
             self.proc = None
         return self
 
@@ -113,7 +113,7 @@ class ClockSampler:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
-            except Exception:
+            except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.out.close()
 
@@ -185,7 +185,7 @@ def oracle_caches(wl, append=False):
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
-    except Exception:
+    except (AttributeError, OSError):                        # not available on this platform
         return os.cpu_count() or 1
 
 
