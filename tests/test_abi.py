@@ -122,6 +122,18 @@ def test_workspace_sizes():
     assert kvq.kvq_decode_workspace_bytes(k, v, 24, 0, 32768) == 0
 
 
+@pytest.mark.parametrize("n_seq,L,n_q", [(1, 32768, 1), (1, 65536, 1), (1, 196608, 1), (1, 1000, 3),
+                                         (16, 65536, 3), (1, 32768, 512)])
+def test_default_splits_leave_no_split_empty(n_seq, L, n_q):
+    """Splits are whole 64-token tiles; the default count is one that every
+    split of the longest sequence gets a tile of."""
+    k, v = _fake_cache(n_seq=n_seq, capacity=-(-L // 64) * 64), _fake_cache(n_seq=n_seq, capacity=-(-L // 64) * 64)
+    s = kvq.kvq_decode_default_splits(k, v, 24, n_q, L)
+    tiles = -(-L // 64)
+    per_split = -(-tiles // s)
+    assert 1 <= s <= tiles and -(-tiles // per_split) == s
+
+
 def test_merge_rejects_bad_arguments():
     lib = kvq._lib
     assert lib.kvq_merge_splits(4096, 4096, 0, 4, 256, 4096, None, None) == kvq.KVQ_EINVAL
