@@ -13,6 +13,10 @@ tokens per step / step time, plus microseconds per generated token.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
+The same JSON line carries, under ``also``, the attention measurements of the
+other long-context workloads (196,608 keys, the 16-sequence MTP verify batch,
+the mixed q8_0-K pair at 65,536 keys), taken the same way in the same run.
+
 ``--impl reference`` times the CPU oracle (fp64 attention over the dequantized
 cache) on the host cores, on the same workload.  Under torchrun each rank runs
 an independent replica (the work is data-parallel across sequences; there is
@@ -183,10 +187,44 @@ def oracle_caches(wl, append=False):
 
 
 def cpu_threads() -> int:
+    """Host cores this process may run on."""
     try:
         return len(os.sched_getaffinity(0))
     except (AttributeError, OSError):                        # not available on this platform
         return os.cpu_count() or 1
+
+
+def oracle_threads() -> int:
+    """Threads the oracle runs with on all host cores: one per core, spread over
+    (sequence, kv head, query row) items."""
+    return cpu_threads()
+
+
+def time_oracle(wl, k, v, threads, budget_s, max_steps):
+    """Mean seconds of whole oracle steps, repeated until about budget_s."""
+    n, total = 0, 0.0
+    while (n == 0 or total < budget_s) and n < max_steps:
+        total += oracle_step_time(wl, k, v, threads)
+        n += 1
+    return total / n, n, total
+
+
+def cpu_baseline(wl, kv_bytes, budget_s=10.0, max_steps=1000):
+    """The oracle timed on the host cores, single-threaded and on all cores."""
+    import oracle
+    oracle.build()
+    k, v = oracle_caches(wl)
+    host = cpu_threads()
+    threads = oracle_threads()
+    t1, n1, tot1 = time_oracle(wl, k, v, 1, budget_s, max_steps)
+    tn, nn, totn = time_oracle(wl, k, v, threads, budget_s, max_steps)
+    step = f"full {wl.spec.name} steps (append + fp64 attention over {int(wl.kv_len.sum())} tokens)"
+    return {"value": round(kv_bytes / tn / 1e9, 4), "unit": "GB/s", "cores": threads, "host_cores": host,
+            "threads": threads, "kind": "oracle",
+            "sample": f"{nn} {step} on {threads} threads, {totn:.1f} s",
+            "single_thread": {"value": round(kv_bytes / t1 / 1e9, 4), "unit": "GB/s", "threads": 1,
+                              "sample": f"{n1} {step} on 1 thread, {tot1:.1f} s"},
+            "all_cores": {"value": round(kv_bytes / tn / 1e9, 4), "unit": "GB/s", "threads": threads}}
 
 
 def run_reference(args, wl, kv_bytes):
@@ -194,8 +232,7 @@ def run_reference(args, wl, kv_bytes):
     import oracle
     oracle.build()
     k, v = oracle_caches(wl)
-    units = wl.spec.n_seq * wl.spec.n_kv_heads
-    threads = max(1, min(cpu_threads(), units))
+    threads = oracle_threads()
     for _ in range(args.warmup):
         oracle_step_time(wl, k, v, threads)
     times = [oracle_step_time(wl, k, v, threads) for _ in range(args.steps)]
@@ -207,8 +244,8 @@ def run_reference(args, wl, kv_bytes):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy Gaussian K/V/Q; no dataset or weights)",
             "config": _config(wl, args),
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "host_cores": cpu_threads(),
+                             "threads": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -227,222 +264,299 @@ def _config(wl, args, extra=None):
     return c
 
 
+class Session:
+    """One workload resident on the GPU: its caches (rotating copies, so that
+    every step reads its cache from HBM), the step's inputs and outputs, and
+    CUDA graphs of its decode steps."""
+
+    def __init__(self, wl, kv_bytes, args, dev, dist):
+        import torch
+        import quantized_kv_cache_q4_gb300 as kvq
+        self.torch, self.kvq, self.wl, self.kv_bytes, self.args, self.dev, self.dist = (
+            torch, kvq, wl, kv_bytes, args, dev, dist)
+        sp = wl.spec
+        S, Hk, D, H, nq = sp.n_seq, sp.n_kv_heads, sp.head_dim, sp.n_heads, sp.n_q
+        self.S, self.D, self.H, self.nq = S, D, H, nq
+
+        def to_dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        # resident cache: prefill through the library's own quantizer
+        k0 = kvq.KVCache(sp.k_codec, S, Hk, D, wl.capacity, device=dev)
+        v0 = kvq.KVCache(sp.v_codec, S, Hk, D, wl.capacity, device=dev)
+        zero = torch.zeros(1, dtype=torch.int32, device=dev)
+        for s in range(S):
+            L = int(wl.cached_len[s])
+            kvq.kvq_quantize_append(k0.seq_view(s), v0.seq_view(s), to_dev(wl.k_prefill[s][None]),
+                                    to_dev(wl.v_prefill[s][None]), L, zero)
+        torch.cuda.synchronize()
+        self.cache_bytes = k0.nbytes() + v0.nbytes()
+        # rotating copies so that every step reads its cache from HBM, not L2
+        self.n_copies = max(1, min(64, math.ceil(4 * L2_BYTES / max(1, kv_bytes))))
+        self.caches = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(self.n_copies - 1)]
+
+        # the step's inputs (new K/V rows, q) are views of one device buffer and
+        # its results (out, lse) of another, so that the end-to-end legs move
+        # each direction with one copy; every view starts on a 256-byte boundary
+        def layout(arrays):
+            offs, o = [], 0
+            for a in arrays:
+                offs.append(o)
+                o += -(-a.nbytes // 256) * 256
+            return offs, o
+        in_arrays = [np.ascontiguousarray(a) for a in (wl.k_new, wl.v_new, wl.q)]
+        in_offs, in_bytes = layout(in_arrays)
+        self.stage_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        self.h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+        views = []
+        for a, o in zip(in_arrays, in_offs):
+            t = torch.from_numpy(a)
+            self.h_in[o:o + a.nbytes].copy_(t.reshape(-1).view(torch.uint8))
+            views.append(self.stage_in[o:o + a.nbytes].view(t.dtype).view(t.shape))
+        self.stage_in.copy_(self.h_in)
+        self.k_new, self.v_new, self.q = views
+        self.pos0, self.kv_len = to_dev(wl.cached_len), to_dev(wl.kv_len)
+        self.max_kv = int(wl.kv_len.max())
+        self.n_splits = args.splits if args.splits is not None else 0
+        self.n_splits_eff = self.n_splits or kvq.kvq_decode_default_splits(k0, v0, H, nq, self.max_kv)
+        self.ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(k0, v0, H, nq, self.max_kv, self.n_splits), dev)
+        self.n_out, n_lse = S * nq * H * D, S * nq * H
+        self.lse_off = -(-self.n_out // 64) * 64
+        self.stage_out = torch.empty(self.lse_off + n_lse, dtype=torch.float32, device=dev)
+        self.out = self.stage_out[:self.n_out].view(S, nq, H, D)
+        self.lse = self.stage_out[self.lse_off:self.lse_off + n_lse].view(S, nq, H)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+
+        # CUDA graphs, so that the host is not on the timed path: one per cache
+        # copy (one step) and one for a round of n_copies consecutive steps, one
+        # per copy, as an engine captures a whole decode step of many layers
+        with torch.cuda.stream(self.stream):
+            for i in range(self.n_copies):      # warm the launch path before capture
+                self.step(i)
+        self.stream.synchronize()
+        self.graphs = []
+        for i in range(self.n_copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.step(i)
+            self.graphs.append(g)
+        self.round_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.round_graph, stream=self.stream):
+            for i in range(self.n_copies):
+                self.step(i)
+        torch.cuda.synchronize()
+        assert int(self.err.item()) == 0, "device error bits set during set-up"
+
+    def step(self, i, ev=None, res=None):
+        """One decode step on cache copy i: append the new rows, then attention."""
+        kvq, sp = self.kvq, self.wl.spec
+        kc, vc = self.caches[i % self.n_copies]
+        o_, l_ = res if res is not None else (self.out, self.lse)
+        kvq.kvq_quantize_append(kc, vc, self.k_new, self.v_new, self.nq, self.pos0, self.err, stream=self.stream)
+        if ev is not None:
+            ev[0].record(self.stream)
+        kvq.kvq_decode_attention(kc, vc, self.q, self.nq, self.H, sp.scale, self.kv_len, self.max_kv, self.n_splits,
+                                 o_, l_, self.ws, d_err=self.err, stream=self.stream)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def replay_steps(self, n):
+        """Exactly n steps: whole rounds, then single steps."""
+        for _ in range(n // self.n_copies):
+            self.round_graph.replay()
+        for i in range(n % self.n_copies):
+            self.graphs[i].replay()
+
+    def barrier(self):
+        self.torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def timed_steps(self, steps, soak_s, local):
+        """Milliseconds per step over exactly `steps` graph-replayed steps
+        (max over ranks), with the clocks sampled from a soak of the same
+        replays through the timed region."""
+        torch = self.torch
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clocks:
+            t_soak = time.perf_counter()
+            with torch.cuda.stream(self.stream):
+                while time.perf_counter() - t_soak < soak_s:
+                    self.replay_steps(64)
+                    self.stream.synchronize()
+            self.barrier()
+            with torch.cuda.stream(self.stream):
+                t_start.record(self.stream)
+                self.replay_steps(steps)
+                t_end.record(self.stream)
+            self.barrier()
+        ms = reduce_max(t_start.elapsed_time(t_end) / steps, self.dist, self.dev)
+        return ms, clocks.summary()
+
+    def attention_eager_ms(self):
+        """The attention call alone, eager, with events around each call on its
+        stream; a sleep kernel holds the stream while the host enqueues a batch
+        of eager steps, so host launch time never shows up between the events."""
+        torch = self.torch
+        attn_ms = []
+        reps = max(1, min(20, self.args.steps // self.n_copies))
+        for _ in range(reps):
+            evs = []
+            with torch.cuda.stream(self.stream):
+                torch.cuda._sleep(int(4e6))
+                for i in range(self.n_copies):
+                    e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    self.step(i, e)
+                    evs.append(e)
+            self.stream.synchronize()
+            attn_ms += [a.elapsed_time(b) for a, b in evs]
+        return statistics.median(attn_ms)
+
+    def attention_graph_ms(self):
+        """The attention kernels as a pipelined engine runs them: a graph of one
+        attention call per cache copy, back to back (each merge chains into the
+        next decode), timed with events around whole replays; per call =
+        total / (replays * copies).  Returns (ms, replays)."""
+        torch, kvq, sp = self.torch, self.kvq, self.wl.spec
+        attn_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(attn_graph, stream=self.stream):
+            for i in range(self.n_copies):
+                kc, vc = self.caches[i]
+                kvq.kvq_decode_attention(kc, vc, self.q, self.nq, self.H, sp.scale, self.kv_len, self.max_kv,
+                                         self.n_splits, self.out, self.lse, self.ws, d_err=self.err,
+                                         stream=self.stream)
+        a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_reps = max(3, self.args.steps // self.n_copies)
+        with torch.cuda.stream(self.stream):
+            for _ in range(2):
+                attn_graph.replay()
+            a_start.record(self.stream)
+            for _ in range(a_reps):
+                attn_graph.replay()
+            a_end.record(self.stream)
+        self.stream.synchronize()
+        return reduce_max(a_start.elapsed_time(a_end) / (a_reps * self.n_copies), self.dist, self.dev), a_reps
+
+    def e2e_graph_ms(self, steps, warmup):
+        """End to end through the public API, steps replayed from graphs: new
+        K/V rows and q from pinned host memory (one copy of the staging buffer);
+        the results written by the kernels straight into pinned, device-mapped
+        host memory (out and lse are host pointers there); one synchronisation
+        a step.  Returns (ms, h2d bytes, d2h bytes, host results)."""
+        torch = self.torch
+        h_res = torch.zeros(self.stage_out.shape, dtype=self.stage_out.dtype).pin_memory()
+        h_out = h_res[:self.n_out].view(self.out.shape)
+        h_lse = h_res[self.lse_off:self.lse_off + self.lse.numel()].view(self.lse.shape)
+        e2e_graphs = []
+        for i in range(self.n_copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.stage_in.copy_(self.h_in, non_blocking=True)
+                self.step(i, res=(h_out, h_lse))
+            e2e_graphs.append(g)
+        # each replay is launched on the stream and waited for before the next one
+        with torch.cuda.stream(self.stream):
+            for i in range(warmup):
+                e2e_graphs[i % self.n_copies].replay()
+                self.stream.synchronize()
+        self.barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            for i in range(steps):
+                e2e_graphs[i % self.n_copies].replay()
+                self.stream.synchronize()
+        ms = reduce_max((time.perf_counter() - t0) * 1e3 / steps, self.dist, self.dev)
+        return ms, self.h_in.numel(), h_res.numel() * h_res.element_size(), (h_out, h_lse)
+
+    def e2e_eager_ms(self, steps, warmup):
+        """End to end through the public API with no graph: every step copies the
+        new K/V rows and q from pinned host memory, calls kvq_quantize_append and
+        kvq_decode_attention (argument checks, split choice and launches on the
+        host each time), copies out and lse back to pinned host memory and
+        synchronises once.  Returns (ms, host results)."""
+        torch = self.torch
+        h_res = torch.zeros(self.stage_out.shape, dtype=self.stage_out.dtype).pin_memory()
+
+        def one(i):
+            self.stage_in.copy_(self.h_in, non_blocking=True)
+            self.step(i)
+            h_res.copy_(self.stage_out, non_blocking=True)
+            self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            for i in range(warmup):
+                one(i)
+        self.barrier()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            for i in range(steps):
+                one(i)
+        ms = reduce_max((time.perf_counter() - t0) * 1e3 / steps, self.dist, self.dev)
+        h_out = h_res[:self.n_out].view(self.out.shape)
+        h_lse = h_res[self.lse_off:self.lse_off + self.lse.numel()].view(self.lse.shape)
+        return ms, (h_out, h_lse)
+
+
+def attention_summary(sess, attn_ms, attn_eager_ms, step_ms, clocks, peak):
+    """The attention measurements of one workload (for the ``also`` entries)."""
+    sp = sess.wl.spec
+    kv = sess.kv_bytes
+    gbs = kv / (attn_ms * 1e-3) / 1e9
+    return {"workload": sp.name, "kv_bytes_per_step": kv, "total_kv_tokens": int(sess.wl.kv_len.sum()),
+            "n_splits": sess.n_splits_eff, "attention_us": round(attn_ms * 1e3, 3),
+            "attention_us_eager_call": round(attn_eager_ms * 1e3, 3), "attention_gbs": round(gbs, 2),
+            "frac": round(gbs / peak, 4), "step_us": round(step_ms * 1e3, 3),
+            "step_gbs": round(kv / (step_ms * 1e-3) / 1e9, 2),
+            "us_per_token": round(step_ms * 1e3 / (sp.n_seq * sp.n_q), 4), "clocks": clocks,
+            "l2": f"{sess.n_copies} rotating cache copies, steps replayed from CUDA graphs"}
+
+
 def run_ours(args, wl, kv_bytes, world, rank, local):
     import torch
-    import quantized_kv_cache_q4_gb300 as kvq
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     sp = wl.spec
-    S, Hk, D, H, nq = sp.n_seq, sp.n_kv_heads, sp.head_dim, sp.n_heads, sp.n_q
-
-    def to_dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    # resident cache: prefill through the library's own quantizer
-    k0 = kvq.KVCache(sp.k_codec, S, Hk, D, wl.capacity, device=dev)
-    v0 = kvq.KVCache(sp.v_codec, S, Hk, D, wl.capacity, device=dev)
-    zero = torch.zeros(1, dtype=torch.int32, device=dev)
-    for s in range(S):
-        L = int(wl.cached_len[s])
-        kvq.kvq_quantize_append(k0.seq_view(s), v0.seq_view(s), to_dev(wl.k_prefill[s][None]),
-                                to_dev(wl.v_prefill[s][None]), L, zero)
-    torch.cuda.synchronize()
-    cache_bytes = k0.nbytes() + v0.nbytes()
-    # rotating copies so that every step reads its cache from HBM, not L2
-    n_copies = max(1, min(64, math.ceil(4 * L2_BYTES / max(1, kv_bytes))))
-    caches = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(n_copies - 1)]
-
-    # the step's inputs (new K/V rows, q) are views of one device buffer and its
-    # results (out, lse) of another, so that the end-to-end leg below moves each
-    # direction with one copy; every view starts on a 256-byte boundary
-    def layout(arrays):
-        offs, o = [], 0
-        for a in arrays:
-            offs.append(o)
-            o += -(-a.nbytes // 256) * 256
-        return offs, o
-    in_arrays = [np.ascontiguousarray(a) for a in (wl.k_new, wl.v_new, wl.q)]
-    in_offs, in_bytes = layout(in_arrays)
-    stage_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
-    views = []
-    for a, o in zip(in_arrays, in_offs):
-        t = torch.from_numpy(a)
-        h_in[o:o + a.nbytes].copy_(t.reshape(-1).view(torch.uint8))
-        views.append(stage_in[o:o + a.nbytes].view(t.dtype).view(t.shape))
-    stage_in.copy_(h_in)
-    k_new, v_new, q = views
-    pos0, kv_len = to_dev(wl.cached_len), to_dev(wl.kv_len)
-    max_kv = int(wl.kv_len.max())
-    n_splits = args.splits if args.splits is not None else 0
-    n_splits_eff = n_splits or kvq.kvq_decode_default_splits(k0, v0, H, nq, max_kv)
-    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(k0, v0, H, nq, max_kv, n_splits), dev)
-    n_out, n_lse = S * nq * H * D, S * nq * H
-    lse_off = -(-n_out // 64) * 64
-    stage_out = torch.empty(lse_off + n_lse, dtype=torch.float32, device=dev)
-    out = stage_out[:n_out].view(S, nq, H, D)
-    lse = stage_out[lse_off:lse_off + n_lse].view(S, nq, H)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    def step(i, ev=None, res=None):
-        kc, vc = caches[i % n_copies]
-        o_, l_ = res if res is not None else (out, lse)
-        kvq.kvq_quantize_append(kc, vc, k_new, v_new, nq, pos0, err, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        kvq.kvq_decode_attention(kc, vc, q, nq, H, sp.scale, kv_len, max_kv, n_splits, o_, l_, ws, d_err=err,
-                                 stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    # CUDA graphs, so that the host is not on the timed path: one per cache copy
-    # (one step) and one for a round of n_copies consecutive steps, one per copy,
-    # as an engine captures a whole decode step of many layers in one graph
-    graphs = []
-    with torch.cuda.stream(stream):
-        for i in range(n_copies):      # warm the launch path before capture
-            step(i)
-    stream.synchronize()
-    for i in range(n_copies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(i)
-        graphs.append(g)
-    round_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(round_graph, stream=stream):
-        for i in range(n_copies):
-            step(i)
-    torch.cuda.synchronize()
-
-    def replay_steps(n):
-        """Exactly n steps: whole rounds, then single steps."""
-        for _ in range(n // n_copies):
-            round_graph.replay()
-        for i in range(n % n_copies):
-            graphs[i].replay()
-    assert int(err.item()) == 0, "device error bits set during set-up"
-
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
         dist = dist_mod
-
-    def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-
-    with torch.cuda.stream(stream):
-        replay_steps(args.warmup)
-    barrier()
+    sess = Session(wl, kv_bytes, args, dev, dist)
+    with torch.cuda.stream(sess.stream):
+        sess.replay_steps(args.warmup)
+    sess.barrier()
 
     # timed region: exactly K steps.  The clock sampler runs from a ~1 s soak of
     # the same replays (part of the warm-up) through the timed region, so the
     # samples are taken under this load with the clocks it settles at.
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        t_soak = time.perf_counter()
-        with torch.cuda.stream(stream):
-            while time.perf_counter() - t_soak < args.soak:
-                replay_steps(64)
-                stream.synchronize()
-        barrier()
-        with torch.cuda.stream(stream):
-            t_start.record(stream)
-            replay_steps(args.steps)
-            t_end.record(stream)
-        barrier()
-    ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dist, dev)
-    clock_summary = clocks.summary()
-
-    # the attention call alone (its kernels), timed with events on its stream.
-    # A sleep kernel holds the stream while the host enqueues a batch of eager
-    # steps, so host launch time never shows up between the two events.
-    attn_ms = []
-    reps = max(1, min(20, args.steps // n_copies))
-    for rep in range(reps):
-        evs = []
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(4e6))
-            for i in range(n_copies):
-                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                step(i, e)
-                evs.append(e)
-        stream.synchronize()
-        attn_ms += [a.elapsed_time(b) for a, b in evs]
-    attn_eager = statistics.median(attn_ms)
-
-    # the attention kernels as a pipelined engine runs them: a graph of one
-    # attention call per cache copy, back to back (each merge chains into the
-    # next decode), timed with events around whole replays; per call = / copies
-    attn_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(attn_graph, stream=stream):
-        for i in range(n_copies):
-            kc, vc = caches[i]
-            kvq.kvq_decode_attention(kc, vc, q, nq, H, sp.scale, kv_len, max_kv, n_splits, out, lse, ws,
-                                     d_err=err, stream=stream)
-    a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a_reps = max(3, args.steps // n_copies)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            attn_graph.replay()
-        a_start.record(stream)
-        for _ in range(a_reps):
-            attn_graph.replay()
-        a_end.record(stream)
-    stream.synchronize()
-    attn = reduce_max(a_start.elapsed_time(a_end) / (a_reps * n_copies), dist, dev)
-
-    # end to end through the public API: new K/V rows and q from pinned host
-    # memory (one copy of the staging buffer); the results written by the
-    # kernels straight into pinned, device-mapped host memory (out and lse are
-    # host pointers there); one synchronisation a step
-    h_res = torch.zeros(stage_out.shape, dtype=stage_out.dtype).pin_memory()
-    h_out = h_res[:n_out].view(S, nq, H, D)
-    h_lse = h_res[lse_off:lse_off + n_lse].view(S, nq, H)
-    e2e_graphs = []
-    for i in range(n_copies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            stage_in.copy_(h_in, non_blocking=True)
-            step(i, res=(h_out, h_lse))
-        e2e_graphs.append(g)
-    # each replay is launched on `stream` and waited for before the next one
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_graphs[i % n_copies].replay()
-            stream.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            e2e_graphs[i % n_copies].replay()
-            stream.synchronize()
-    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / args.steps, dist, dev)
+    ms, clock_summary = sess.timed_steps(args.steps, args.soak, local)
+    attn_eager = sess.attention_eager_ms()
+    attn, a_reps = sess.attention_graph_ms()
+    e2e_ms, h2d, d2h, (h_out, h_lse) = sess.e2e_graph_ms(args.steps, args.warmup)
     # the host copy holds what the device-resident path computes
-    assert torch.equal(h_out, out.cpu()) and torch.equal(h_lse, lse.cpu()), "end-to-end results differ"
-    h2d = h_in.numel() * h_in.element_size()
-    d2h = h_res.numel() * h_res.element_size()
-    assert int(err.item()) == 0, "device error bits set during the run"
+    assert torch.equal(h_out, sess.out.cpu()) and torch.equal(h_lse, sess.lse.cpu()), "end-to-end results differ"
+    eager_ms, (e_out, e_lse) = sess.e2e_eager_ms(args.steps, args.warmup)
+    assert torch.equal(e_out, sess.out.cpu()) and torch.equal(e_lse, sess.lse.cpu()), "eager results differ"
+    assert int(sess.err.item()) == 0, "device error bits set during the run"
 
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (attn * 1e-3) / 1e9
     value = job_gbs(kv_bytes, ms, world)
     # kernels launched per step: append + decode (+ merge when the range is split)
-    launches = args.steps * (2 + (1 if n_splits_eff > 1 else 0))
+    per_step = 2 + (1 if sess.n_splits_eff > 1 else 0)
+    launches = args.steps * per_step
     tokens_per_step = sp.n_seq * sp.n_q
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded numpy Gaussian K/V/Q; no dataset or weights)",
-        "config": _config(wl, args, {"n_splits": n_splits_eff, "kv_bytes_per_step": kv_bytes,
-                                     "cache_bytes": cache_bytes,
-                                     "l2": f"{n_copies} rotating cache copies ({n_copies * cache_bytes / 1e6:.0f} MB, "
-                                           f">= 4x the 129 MB L2); steps replayed from CUDA graphs of {n_copies} "
-                                           f"consecutive steps, one per copy",
+        "config": _config(wl, args, {"n_splits": sess.n_splits_eff, "kv_bytes_per_step": kv_bytes,
+                                     "cache_bytes": sess.cache_bytes,
+                                     "l2": f"{sess.n_copies} rotating cache copies "
+                                           f"({sess.n_copies * sess.cache_bytes / 1e6:.0f} MB, >= 4x the 129 MB "
+                                           f"L2); steps replayed from CUDA graphs of {sess.n_copies} consecutive "
+                                           f"steps, one per copy",
                                      "parallelism": f"replicas x{world}",
                                      "arithmetic": "int4/int8 codes as exact fp16 MMA operands, fp32 accumulate, "
                                                    "fp32 softmax"}),
@@ -452,14 +566,48 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": _traffic(sp.name), "attention_us": round(attn * 1e3, 3),
-                     "attention_timing": f"graph of {n_copies} back-to-back calls, events around {a_reps} replays",
+                     "attention_timing": f"graph of {sess.n_copies} back-to-back calls, events around {a_reps} "
+                                         f"replays",
                      "attention_us_eager_call": round(attn_eager * 1e3, 3)},
         "e2e": {"value": round(job_gbs(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6),
+                "path": "steps replayed from CUDA graphs of the public calls; one synchronisation a step"},
+        "e2e_eager": {"value": round(job_gbs(kv_bytes, eager_ms, world), 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(eager_ms, 6),
+                      "path": "kvq_quantize_append + kvq_decode_attention called eagerly every step, host copies "
+                              "in and out, one synchronisation a step"},
         "gpu_launches": launches,
         "clocks": clock_summary,
     }
+    del sess
+    torch.cuda.empty_cache()
+
+    # the other long-context workloads, measured the same way in the same run
+    if not args.no_also:
+        also = {}
+        for cfg in ALSO_CONFIGS:
+            if cfg == args.config:
+                continue
+            wl2 = workloads.make(workloads.spec(cfg))
+            kv2 = workloads.kv_bytes_per_token(wl2.spec) * int(wl2.kv_len.sum())
+            s2 = Session(wl2, kv2, args, dev, dist)
+            with torch.cuda.stream(s2.stream):
+                s2.replay_steps(args.warmup)
+            s2.barrier()
+            ms2, clocks2 = s2.timed_steps(args.steps, min(args.soak, 0.5), local)
+            eager2 = s2.attention_eager_ms()
+            attn2, _ = s2.attention_graph_ms()
+            assert int(s2.err.item()) == 0, "device error bits set during the run"
+            also[wl2.spec.name] = attention_summary(s2, attn2, eager2, ms2, clocks2, peak)
+            del s2
+            torch.cuda.empty_cache()
+        res["also"] = also
     return res
+
+
+# workloads measured beside the main one: 196,608 keys, the 16-sequence MTP
+# verify batch, the mixed q8_0-K / Q4_G64-V pair at 65,536 keys
+ALSO_CONFIGS = (3, 4, 2)
 
 
 def main():
@@ -473,6 +621,7 @@ def main():
     ap.add_argument("--ref-steps", type=int, default=None, help="oracle steps for the cpu_baseline leg")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed replays before the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true", help="measure the selected workload only")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = _dist_env()
@@ -494,21 +643,7 @@ def main():
         dist.init_process_group("nccl")
     res = run_ours(args, wl, kv_bytes, world, rank, local)
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        k, v = oracle_caches(wl)
-        units = wl.spec.n_seq * wl.spec.n_kv_heads
-        threads = max(1, min(cpu_threads(), units))
-        n, total = 0, 0.0
-        budget = 10.0
-        while total < budget and n < (args.ref_steps or 1000):
-            total += oracle_step_time(wl, k, v, threads)
-            n += 1
-        t = total / n
-        res["cpu_baseline"] = {"value": round(kv_bytes / t / 1e9, 4), "unit": "GB/s", "cores": threads,
-                               "kind": "oracle",
-                               "sample": f"{n} full {wl.spec.name} steps (append + fp64 attention over "
-                                         f"{int(wl.kv_len.sum())} tokens), {total:.1f} s"}
+        res["cpu_baseline"] = cpu_baseline(wl, kv_bytes, max_steps=args.ref_steps or 1000)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

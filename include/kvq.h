@@ -195,6 +195,10 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v,
                                 void *stream);
 
 /* Log-sum-exp merge of partial attention results (one per split of the key range).
+ * The source pages do not describe splitting the key range: this call is the
+ * merge step of the library's own split-K decomposition (kvq_decode_attention
+ * splits long ranges across CTAs), exposed for callers that split themselves,
+ * e.g. a sequence sharded across devices.
  *   part_o   : DEVICE fp32 [n_splits][rows][head_dim], each part normalised over its keys.
  *   part_lse : DEVICE fp32 [n_splits][rows]; -inf marks an empty part (its part_o is ignored).
  *   out      : DEVICE fp32 [rows][head_dim] = sum_s w_s part_o[s] / sum_s w_s with
@@ -213,10 +217,14 @@ kvq_status kvq_merge_splits(const float *part_o, const float *part_lse, int32_t 
  * Arguments, results and errors are those of kvq_decode_attention; the split
  * scratch comes from a file-scope __device__ array of KVQ_STATIC_SCRATCH_BYTES
  * inside libkvq.so, which every GPU that loads the library keeps until the
- * process exits.  A call whose scratch (kvq_decode_workspace_bytes with the
- * same arguments) exceeds that size returns KVQ_EWORKSPACE before touching the
- * GPU.  The first call on each device looks up the array's device address
- * (with that device current); make that first call before any stream capture.
+ * process exits.  With n_splits = 0 the split count is lowered, if needed, to
+ * the largest one whose scratch fits the array; an explicit n_splits whose
+ * scratch (kvq_decode_workspace_bytes with the same arguments) exceeds that
+ * size returns KVQ_EWORKSPACE before anything is launched.  The first call in
+ * each CUDA context looks up the array's device address (with that context's
+ * device current) and keeps it for that context; make that first call before
+ * any stream capture.  After cudaDeviceReset (a new context) the next call
+ * looks the address up again.
  * Every call on a device shares the one array and leaves its contents behind:
  * nothing in it needs to start at zero, but two calls that overlap on the GPU
  * (different streams, no ordering between them) race on it and give wrong

@@ -383,15 +383,17 @@ typedef struct {
     double scale;
 } orc_attn_args;
 
-/* Softmax attention of every query row of (s, kv head kh) over the tokens
- * [t_lo, t_hi) intersected with each row's visible range.  Writes, for each
- * row, the output normalised over that range and its log-sum-exp; a row with
- * no token in range gets o = 0 and lse = -inf.
+/* Softmax attention of the query rows [r_lo, r_hi) of (s, kv head kh) over
+ * the tokens [t_lo, t_hi) intersected with each row's visible range.  Writes,
+ * for each of those rows r, the output normalised over that range and its
+ * log-sum-exp at o + r * stride and lse + r * stride (rows outside the range
+ * are not touched); a row with no token in range gets o = 0 and lse = -inf.
  * Query head h uses kv head h / (n_heads / n_kv_heads).  Two passes: scores
- * and their maximum, then exp, sum and the weighted sum of V rows. */
-static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo, int64_t t_hi,
-                            double *o, double *lse, int64_t o_row_stride_elems,
-                            int64_t lse_row_stride)
+ * and their maximum, then exp, sum and the weighted sum of V rows.  Each row's
+ * arithmetic depends on that row alone, so any row range gives the same
+ * values for its rows. */
+static void orc_attend_rows(const orc_attn_args *a, int s, int kh, int64_t t_lo, int64_t t_hi, int r_lo,
+                            int r_hi, double *o, double *lse, int64_t o_row_stride_elems, int64_t lse_row_stride)
 {
     int D = a->head_dim, G = a->n_heads / a->n_kv_heads, R = a->n_q * G;
     int64_t span = t_hi > t_lo ? t_hi - t_lo : 0;
@@ -408,6 +410,7 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     for (int i = 0; i < a->n_q; ++i)
         for (int j = 0; j < G; ++j) {
             int r = i * G + j, h = kh * G + j;
+            if (r < r_lo || r >= r_hi) continue;
             const float *qv = a->q + (((int64_t)s * a->n_q + i) * a->n_heads + h) * D;
             for (int d = 0; d < D; ++d) qd[r * D + d] = (double)qv[d];
             int64_t vis = orc_visible(a->kv_len[s], a->n_q, i);
@@ -420,7 +423,7 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     for (int64_t t = 0; t < span; ++t) {
         int64_t row = plane + t_lo + t;
         orc_dequantize(a->k_codec, a->k_qs + row * krb, a->k_sc + row * ksb, 1, D, kr);
-        for (int r = 0; r < R; ++r) {
+        for (int r = r_lo; r < r_hi; ++r) {
             if (t >= nv[r]) continue;
             double acc = 0.0;
             for (int d = 0; d < D; ++d) acc += qd[r * D + d] * (double)kr[d];
@@ -429,7 +432,7 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     }
     double *m = (double *)malloc(sizeof(double) * (size_t)R);
     double *l = (double *)malloc(sizeof(double) * (size_t)R);
-    for (int r = 0; r < R; ++r) {
+    for (int r = r_lo; r < r_hi; ++r) {
         m[r] = -INFINITY;
         for (int64_t t = 0; t < nv[r]; ++t) if (z[r * span + t] > m[r]) m[r] = z[r * span + t];
         l[r] = 0.0;
@@ -444,17 +447,17 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
     for (int64_t t = 0; t < span; ++t) {
         int64_t row = plane + t_lo + t;
         int need = 0;
-        for (int r = 0; r < R; ++r) need |= (t < nv[r]);
+        for (int r = r_lo; r < r_hi; ++r) need |= (t < nv[r]);
         if (!need) continue;
         orc_dequantize(a->v_codec, a->v_qs + row * vrb, a->v_sc + row * vsb, 1, D, vr);
-        for (int r = 0; r < R; ++r) {
+        for (int r = r_lo; r < r_hi; ++r) {
             if (t >= nv[r]) continue;
             double p = z[r * span + t];
             double *orow = o + (int64_t)r * o_row_stride_elems;
             for (int d = 0; d < D; ++d) orow[d] += p * (double)vr[d];
         }
     }
-    for (int r = 0; r < R; ++r) {
+    for (int r = r_lo; r < r_hi; ++r) {
         double *orow = o + (int64_t)r * o_row_stride_elems;
         if (nv[r] == 0) { lse[(int64_t)r * lse_row_stride] = -INFINITY; continue; }
         for (int d = 0; d < D; ++d) orow[d] /= l[r];
@@ -468,14 +471,15 @@ static void orc_attend_unit(const orc_attn_args *a, int s, int kh, int64_t t_lo,
  * a stride; query token i of the unit starts G rows further in the unit but
  * n_heads rows further in the output, so the unit is run per query token. */
 static void orc_attend_unit_to_output(const orc_attn_args *a, int s, int kh, int64_t t_lo,
-                                      int64_t t_hi, double *out, double *out_lse)
+                                      int64_t t_hi, int r_lo, int r_hi, double *out, double *out_lse)
 {
     int D = a->head_dim, G = a->n_heads / a->n_kv_heads, R = a->n_q * G;
     double *o = (double *)malloc(sizeof(double) * (size_t)(R * D));
     double *l = (double *)malloc(sizeof(double) * (size_t)R);
-    orc_attend_unit(a, s, kh, t_lo, t_hi, o, l, D, 1);
+    orc_attend_rows(a, s, kh, t_lo, t_hi, r_lo, r_hi, o, l, D, 1);
     for (int i = 0; i < a->n_q; ++i)
         for (int j = 0; j < G; ++j) {
+            if (i * G + j < r_lo || i * G + j >= r_hi) continue;
             int64_t orow = ((int64_t)s * a->n_q + i) * a->n_heads + kh * G + j;
             memcpy(out + orow * D, o + (int64_t)(i * G + j) * D, sizeof(double) * (size_t)D);
             out_lse[orow] = l[i * G + j];
@@ -485,8 +489,9 @@ static void orc_attend_unit_to_output(const orc_attn_args *a, int s, int kh, int
 
 /* Full decode attention: out [n_seq][n_q][n_heads][head_dim] fp64,
  * out_lse [n_seq][n_q][n_heads] fp64 (natural log).  q is fp32 (the fp16 or
- * fp32 inputs widened exactly).  n_threads > 1 spreads (seq, kv head) units
- * over OpenMP threads; the arithmetic per unit is unchanged. */
+ * fp32 inputs widened exactly).  n_threads > 1 spreads (seq, kv head, query
+ * row) items over OpenMP threads; the arithmetic of each row is the same
+ * whichever thread computes it. */
 void orc_decode_attention(int k_codec, const uint8_t *k_qs, const void *k_sc,
                           int v_codec, const uint8_t *v_qs, const void *v_sc,
                           int n_seq, int n_kv_heads, int head_dim, int capacity,
@@ -495,14 +500,25 @@ void orc_decode_attention(int k_codec, const uint8_t *k_qs, const void *k_sc,
 {
     orc_attn_args a = {k_codec, v_codec, k_qs, v_qs, (const uint8_t *)k_sc, (const uint8_t *)v_sc, n_seq, n_kv_heads, head_dim,
                        capacity, q, n_q, n_heads, kv_len, scale};
-    int units = n_seq * n_kv_heads;
+    int R = n_q * (n_heads / n_kv_heads);
+    if (n_threads <= 1) {
+        /* one thread: every row of a (seq, kv head) unit in one pass */
+        for (int u = 0; u < n_seq * n_kv_heads; ++u) {
+            int s = u / n_kv_heads, kh = u % n_kv_heads;
+            int64_t hi = kv_len[s] < 0 ? 0 : kv_len[s];
+            orc_attend_unit_to_output(&a, s, kh, 0, hi, 0, R, out, out_lse);
+        }
+        return;
+    }
+    int64_t items = (int64_t)n_seq * n_kv_heads * R;
 #ifdef _OPENMP
-#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads > 0 ? n_threads : 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
 #endif
-    for (int u = 0; u < units; ++u) {
+    for (int64_t it = 0; it < items; ++it) {
+        int u = (int)(it / R), r = (int)(it % R);
         int s = u / n_kv_heads, kh = u % n_kv_heads;
         int64_t hi = kv_len[s] < 0 ? 0 : kv_len[s];
-        orc_attend_unit_to_output(&a, s, kh, 0, hi, out, out_lse);
+        orc_attend_unit_to_output(&a, s, kh, 0, hi, r, r + 1, out, out_lse);
     }
     (void)n_threads;
 }
@@ -529,8 +545,8 @@ void orc_decode_attention_split(int k_codec, const uint8_t *k_qs, const void *k_
             int64_t lo = sp * chunk, hi = lo + chunk < len ? lo + chunk : len;
             if (lo > hi) lo = hi;
             for (int kh = 0; kh < n_kv_heads; ++kh)
-                orc_attend_unit_to_output(&a, s, kh, lo, hi, part_o + sp * rows * head_dim,
-                                          part_lse + sp * rows);
+                orc_attend_unit_to_output(&a, s, kh, lo, hi, 0, n_q * (n_heads / n_kv_heads),
+                                          part_o + sp * rows * head_dim, part_lse + sp * rows);
         }
 }
 

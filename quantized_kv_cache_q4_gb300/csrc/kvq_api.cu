@@ -62,13 +62,14 @@ kvq::Plane plane_of(const kvq_cache *c)
 
 int sm_count()
 {
-    int dev = 0, n = 0;
+    static kvq::PerDevice pd;
+    int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    static int cached[64] = {0};
-    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
-    return n;
+    const int n = kvq::per_device(pd, dev, [dev]() -> int {
+        int v = 0;
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 0;
+    });
+    return n > 0 ? n : 148;
 }
 
 constexpr int kMaxSplits = 4096;
@@ -84,11 +85,11 @@ int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int3
                    int32_t n_splits)
 {
     if (n_splits > 0) return n_splits;
-    // one CTA per (sequence, kv head, block of query rows) and split
     const int rows = n_q * (n_heads / k->n_kv_heads);
+    // one CTA per (sequence, kv head, block of query rows) and split
     const int64_t units = (int64_t)k->n_seq * k->n_kv_heads * (k->head_dim <= 256 ? kvq::tc_row_blocks(rows) : 1);
     // CTAs of the decode kernel an SM holds (3 where the occupancy is unknown)
-    int per_sm = kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, n_q * (n_heads / k->n_kv_heads));
+    int per_sm = kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, rows);
     if (per_sm <= 0) per_sm = 3;
     int64_t target;
     if (k->n_seq == 1) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <utility>
 
 #include "kvq.h"
@@ -128,6 +130,31 @@ __host__ __device__ inline void split_range(int len, int n_splits, int split, in
     lo = (int)(l < len ? l : len);
     long long h = l + chunk;
     hi = (int)(h < len ? h : len);
+}
+
+// A positive per-device value (kernel occupancy, SM count), computed once per
+// device by `compute` (which returns a value > 0, or <= 0 on failure and is
+// then tried again on the next call).  Safe when several host threads make
+// their first call at the same time: the first computes under a lock, the
+// others wait for it, later calls read one atomic.
+struct PerDevice {
+    static constexpr int kMaxDevices = 64;
+    std::atomic<int> value[kMaxDevices];
+    std::mutex mu;
+};
+
+template <typename F>
+inline int per_device(PerDevice &pd, int dev, F compute)
+{
+    if (dev < 0 || dev >= PerDevice::kMaxDevices) return compute();
+    int v = pd.value[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    std::lock_guard<std::mutex> lock(pd.mu);
+    v = pd.value[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    v = compute();
+    if (v > 0) pd.value[dev].store(v, std::memory_order_release);
+    return v;
 }
 
 // Set the message kvq_last_error() returns on the calling thread.

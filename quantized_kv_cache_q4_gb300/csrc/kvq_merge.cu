@@ -115,15 +115,15 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
     // splits, fewer while that would take more than about a quarter wave of
     // threads (measured on GB300: 114 splits x 24 rows is fastest with 16 lanes,
     // 29 splits x 1152 rows with one lane per column)
-    static int sms[64] = {};
+    static PerDevice pd;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-    int n_sm = (dev >= 0 && dev < 64) ? sms[dev] : 0;
-    if (n_sm <= 0) {
-        if (dev < 0 || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
-            n_sm = 152;
-        if (dev >= 0 && dev < 64) sms[dev] = n_sm;
-    }
+    int n_sm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        n_sm = per_device(pd, dev, [dev]() -> int {
+            int v = 0;
+            return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 0;
+        });
+    if (n_sm <= 0) n_sm = 152;
     int lpc = 1;
     while (lpc < 32 && lpc * 2 * kUnroll < n_splits) lpc *= 2;
     const int64_t items = (int64_t)rows * (head_dim / 4);

@@ -227,7 +227,9 @@ struct TileGeom {
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 
-bool make_codes_map(CUtensorMap *m, void *base, int row_bytes, int64_t rows);
+// TMA descriptor of a codes plane [rows][row_bytes] with boxes of box_rows
+// rows (encoded once per distinct argument set and kept; thread-safe).
+bool make_codes_map(CUtensorMap *m, void *base, int row_bytes, int64_t rows, int box_rows);
 bool tensor_maps_available();
 
 }  // namespace ptx

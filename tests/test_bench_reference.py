@@ -24,3 +24,19 @@ def test_reference_arm_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_cores_and_both_thread_counts():
+    """The CPU baseline times the oracle single-threaded and on all host cores
+    and states the core count it found."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    wl = workloads.make(workloads.spec(0))
+    kv = workloads.kv_bytes_per_token(wl.spec) * int(wl.kv_len.sum())
+    cb = bench.cpu_baseline(wl, kv, budget_s=0.0, max_steps=1)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s"
+    assert cb["host_cores"] == bench.cpu_threads() >= 1
+    assert cb["threads"] == cb["cores"] == bench.oracle_threads()
+    assert cb["single_thread"]["threads"] == 1 and cb["single_thread"]["value"] > 0
+    assert cb["all_cores"]["value"] == cb["value"] > 0

@@ -31,6 +31,18 @@ def test_workload_default_splits(cfg):
     check_close(o, o_ref, lse, lse_ref)
 
 
+def test_long196k_explicit_splits():
+    """The 196,608-key workload at full size with 64 and 256 splits of the key
+    range (besides the default count), each merged by log-sum-exp."""
+    wl = workloads.make(workloads.spec(3))
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale, n_threads=oracle.max_threads())
+    for n_splits in (64, 256):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
 @pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 255, 257])
 @pytest.mark.parametrize("n_new", [1, 2, 3])
 @pytest.mark.parametrize("G", [1, 6])
@@ -72,6 +84,7 @@ def test_codec_pairs(kc, vc, D):
     o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
     for n_splits in (1, 5):
         o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
         check_close(o, o_ref, lse, lse_ref)
 
 
@@ -97,8 +110,10 @@ def test_tensor_core_codec_pairs(kc, vc, G, n_new, D):
                                    (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q4_G32), (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4)])
 @pytest.mark.parametrize("D", [128, 256])
 def test_more_than_32_rows_per_kv_head(kc, vc, D):
-    """12 query heads per kv head x 3 query tokens = 36 rows: past the
-    tensor-core kernel's 32, the SIMT kernel runs."""
+    """12 query heads per kv head x 3 query tokens = 36 rows per kv head: the
+    tensor-core kernel takes them in two blocks of up to 32 rows (32 + 4), one
+    CTA each.  (The CUDA-core kernel serves head_dim 512 only; it is covered by
+    the head_dim-512 cases of test_codec_pairs and test_prompt_chunk.)"""
     wl = workloads.custom(n_seq=2, n_heads=12, n_kv_heads=1, head_dim=D, cached=(600, 77), n_new=3, k_codec=kc,
                           v_codec=vc, src_dtype="f16", q_dtype="f16", seed=5 * kc + vc + D)
     k, v, ko, vo = _both(wl)

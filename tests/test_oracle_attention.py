@@ -196,3 +196,16 @@ def test_merge_closed_forms():
     lmix = np.concatenate([l1, np.full((1, 4), -np.inf)])     # an empty part carries no weight
     om, lm = oracle.merge_splits(np.concatenate([o1, np.full((1, 4, 32), 1e300)]), lmix)
     assert np.array_equal(om, o1[0]) and np.array_equal(lm, l1[0])
+
+
+def test_thread_count_does_not_change_results():
+    """The oracle's threads split (sequence, kv head, query row) items; every
+    row's arithmetic is the same on any thread, so the results are bitwise
+    equal for any thread count."""
+    wl = workloads.custom(n_seq=3, n_heads=12, n_kv_heads=2, head_dim=128, cached=(300, 77, 5), n_new=3,
+                          src_dtype="f16", q_dtype="f16", seed=31)
+    k, v = oracle_caches(wl)
+    o1, l1 = oracle.decode_attention(k, v, wl.q, wl.kv_len, wl.spec.scale, n_threads=1)
+    for n in (2, 3, 8):
+        on, ln = oracle.decode_attention(k, v, wl.q, wl.kv_len, wl.spec.scale, n_threads=n)
+        assert np.array_equal(o1, on) and np.array_equal(l1, ln)
