@@ -237,6 +237,48 @@ kvq_status kvq_decode_attention_static(const kvq_cache *k, const kvq_cache *v,
                                        int32_t n_splits, float *out, float *out_lse, int32_t *d_err,
                                        void *stream);
 
+/* Host-tier KV streaming: decode attention for one sequence whose
+ * authoritative cache lives in pinned host memory, with a bounded device pool
+ * (den_llama.cpp, "Adaptive KV streaming (contributed)": the authoritative KV
+ * tensors in pinned host memory, a bounded CUDA pool shared by resident pages
+ * and a transfer ring, exact attention over the full context).
+ *   k_host, v_host : the caches (n_seq = 1) whose planes are in pinned host
+ *                    memory (cudaHostAlloc / cudaHostRegister); the library
+ *                    only reads them, with cudaMemcpy2DAsync.
+ *   k_dev, v_dev   : device caches of the same codecs and shape holding the
+ *                    same first n_resident tokens (the resident part, read in
+ *                    place); may be NULL when n_resident = 0.
+ *   kv_len         : HOST int, keys visible to the last query token
+ *                    (1 <= kv_len <= capacity of the host caches).
+ *   page_tokens    : keys per streamed page, a positive multiple of
+ *                    KVQ_CAPACITY_ALIGN; tokens n_resident .. kv_len - 1 are
+ *                    streamed in pages through n_slots ring slots.
+ *   ring           : DEVICE buffer of at least kvq_tiered_ring_bytes(), 256-byte
+ *                    aligned (may be NULL when nothing is streamed).
+ *   workspace      : DEVICE buffer of at least kvq_tiered_workspace_bytes(),
+ *                    256-byte aligned (per-part partials and split scratch).
+ *   q, q_dtype, n_q, n_heads, softmax_scale, out, out_lse, d_err: as in
+ *                    kvq_decode_attention (one sequence).
+ * The result equals kvq_decode_attention over the whole cache up to rounding:
+ * the resident prefix and every page are decoded into partials (o, lse) that
+ * one merge combines.  Page copies run on a copy stream the library creates
+ * once per device and joins to `stream` with events, so the copy of a page
+ * overlaps the decode of earlier ones; the copy into a slot waits until the
+ * slot's previous page has been decoded.  Arguments are checked on the host
+ * before anything is enqueued (KVQ_EINVAL / KVQ_EUNSUPPORTED for n_seq != 1 /
+ * KVQ_EWORKSPACE). */
+size_t kvq_tiered_ring_bytes(const kvq_cache *k_host, const kvq_cache *v_host, int32_t page_tokens,
+                             int32_t n_slots);
+size_t kvq_tiered_workspace_bytes(const kvq_cache *k_host, const kvq_cache *v_host, const kvq_cache *k_dev,
+                                  const kvq_cache *v_dev, int32_t n_heads, int32_t n_q, int32_t kv_len,
+                                  int32_t n_resident, int32_t page_tokens);
+kvq_status kvq_decode_attention_tiered(const kvq_cache *k_host, const kvq_cache *v_host,
+                                       const kvq_cache *k_dev, const kvq_cache *v_dev, int32_t n_resident,
+                                       const void *q, int32_t q_dtype, int32_t n_q, int32_t n_heads,
+                                       float softmax_scale, int32_t kv_len, int32_t page_tokens, int32_t n_slots,
+                                       void *ring, size_t ring_bytes, float *out, float *out_lse,
+                                       void *workspace, size_t workspace_bytes, int32_t *d_err, void *stream);
+
 /* Dequantize a whole cache to fp32 [n_seq][n_kv_heads][capacity][head_dim] on
  * the device (scale * code, exact).  For inspection and testing. */
 kvq_status kvq_dequantize(const kvq_cache *c, float *out, void *stream);

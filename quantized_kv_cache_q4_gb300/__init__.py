@@ -59,6 +59,10 @@ def _load():
         "kvq_dequantize": (I32, [C, P, P]),
         "kvq_static_scratch_bytes": (SZ, []),
         "kvq_decode_attention_static": (I32, [C, C, P, I32, I32, I32, F, P, I32, I32, P, P, P, P]),
+        "kvq_tiered_ring_bytes": (SZ, [C, C, I32, I32]),
+        "kvq_tiered_workspace_bytes": (SZ, [C, C, C, C, I32, I32, I32, I32, I32]),
+        "kvq_decode_attention_tiered": (I32, [C, C, C, C, I32, P, I32, I32, I32, F, I32, I32, I32, P, SZ, P, P, P,
+                                              SZ, P, P]),
         "kvq_status_string": (ctypes.c_char_p, [I32]),
         "kvq_last_error": (ctypes.c_char_p, []),
     }
@@ -72,7 +76,8 @@ _lib = _load()
 EXPORTED = ("kvq_row_bytes", "kvq_scales_per_row", "kvq_scale_bytes", "kvq_quantize_append", "kvq_decode_default_splits",
             "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_merge_splits", "kvq_dequantize",
             "kvq_status_string", "kvq_last_error", "kvq_static_scratch_bytes", "kvq_decode_attention_static",
-            "kvq_selftest_bounded_wait")
+            "kvq_selftest_bounded_wait", "kvq_tiered_ring_bytes", "kvq_tiered_workspace_bytes",
+            "kvq_decode_attention_tiered")
 
 
 def _check(status: int):
@@ -142,6 +147,12 @@ class KVCache:
         return KVCache(self.codec, 1, self.n_kv_heads, self.head_dim, self.capacity,
                        qs=self.qs[s:s + 1], scales=self.scales[s:s + 1])
 
+    def to_host(self) -> "KVCache":
+        """A copy whose planes are in pinned host memory (the host tier of a
+        streamed cache; the structure's pointers are host addresses)."""
+        return KVCache(self.codec, self.n_seq, self.n_kv_heads, self.head_dim, self.capacity,
+                       qs=self.qs.cpu().pin_memory(), scales=self.scales.cpu().pin_memory())
+
     def clone(self) -> "KVCache":
         return KVCache(self.codec, self.n_seq, self.n_kv_heads, self.head_dim, self.capacity,
                        qs=self.qs.clone(), scales=self.scales.clone())
@@ -169,6 +180,10 @@ def kvq_quantize_append(k: KVCache | None, v: KVCache | None, k_src, v_src, n_ne
 def _cref(c):
     """A KVCache or a bare kvq_cache structure, as the C pointer argument."""
     return c.c if isinstance(c, KVCache) else ctypes.byref(c)
+
+
+def _cref_opt(c):
+    return None if c is None else _cref(c)
 
 
 def kvq_decode_default_splits(k, v, n_heads: int, n_q: int, max_kv_len: int) -> int:
@@ -213,6 +228,39 @@ def kvq_decode_attention_static(k: KVCache, v: KVCache, q, n_q: int, n_heads: in
     _check(_lib.kvq_decode_attention_static(k.c, v.c, _ptr(q), q_dtype, int(n_q), int(n_heads),
                                             float(softmax_scale), _ptr(d_kv_len), int(max_kv_len), int(n_splits),
                                             _ptr(out), _ptr(out_lse), _ptr(d_err), _stream(stream)))
+
+
+def kvq_tiered_ring_bytes(k_host, v_host, page_tokens: int, n_slots: int) -> int:
+    return int(_lib.kvq_tiered_ring_bytes(_cref(k_host), _cref(v_host), int(page_tokens), int(n_slots)))
+
+
+def kvq_tiered_workspace_bytes(k_host, v_host, k_dev, v_dev, n_heads: int, n_q: int, kv_len: int, n_resident: int,
+                               page_tokens: int) -> int:
+    return int(_lib.kvq_tiered_workspace_bytes(_cref(k_host), _cref(v_host), _cref_opt(k_dev), _cref_opt(v_dev),
+                                               int(n_heads), int(n_q), int(kv_len), int(n_resident),
+                                               int(page_tokens)))
+
+
+def kvq_decode_attention_tiered(k_host: KVCache, v_host: KVCache, k_dev: KVCache | None, v_dev: KVCache | None,
+                                n_resident: int, q, n_q: int, n_heads: int, softmax_scale: float, kv_len: int,
+                                page_tokens: int, n_slots: int, ring, out, out_lse=None, workspace=None,
+                                ring_bytes=None, workspace_bytes=None, d_err=None, stream=None,
+                                q_dtype: int | None = None):
+    """Decode attention for one sequence whose cache planes are in pinned host
+    memory (k_host, v_host); the first n_resident tokens are read from the
+    device caches k_dev, v_dev, the rest streamed in pages of page_tokens
+    through the device ring (see include/kvq.h)."""
+    if q_dtype is None:
+        q_dtype = _dtype_code(q)
+    if ring_bytes is None:
+        ring_bytes = ring.numel() * ring.element_size() if isinstance(ring, torch.Tensor) else 0
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
+    _check(_lib.kvq_decode_attention_tiered(k_host.c, v_host.c, _cref_opt(k_dev), _cref_opt(v_dev), int(n_resident),
+                                            _ptr(q), q_dtype, int(n_q), int(n_heads), float(softmax_scale),
+                                            int(kv_len), int(page_tokens), int(n_slots), _ptr(ring), int(ring_bytes),
+                                            _ptr(out), _ptr(out_lse), _ptr(workspace), int(workspace_bytes),
+                                            _ptr(d_err), _stream(stream)))
 
 
 def kvq_merge_splits(part_o, part_lse, n_splits: int, rows: int, head_dim: int, out, out_lse=None, stream=None):

@@ -126,6 +126,64 @@ void kvq::set_last_error(const char *msg)
     snprintf(g_last_error, sizeof g_last_error, "%s", msg);
 }
 
+kvq_status kvq::fail_msg(kvq_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+int kvq::resolve_decode_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
+                               int32_t max_kv_len, int32_t n_splits)
+{
+    return resolve_splits(k, v, n_heads, n_q, max_kv_len, n_splits);
+}
+
+kvq_status kvq::decode_checked(const kvq_cache *k, const kvq_cache *v, const void *q, int q_dtype, int n_q,
+                               int n_heads, float softmax_scale, const int32_t *d_kv_len, int fixed_len,
+                               int causal_extra, int max_kv_len, int n_splits, float *out, float *out_lse,
+                               void *workspace, int32_t *d_err, cudaStream_t cs)
+{
+    kvq::DecodeArgs a{};
+    a.k = plane_of(k);
+    a.v = plane_of(v);
+    a.q = q;
+    a.n_seq = k->n_seq;
+    a.n_kv_heads = k->n_kv_heads;
+    a.n_heads = n_heads;
+    a.n_q = n_q;
+    a.head_dim = k->head_dim;
+    a.capacity = k->capacity;
+    a.scale_log2 = softmax_scale * kvq::kLog2e;
+    a.kv_len = d_kv_len;
+    a.fixed_len = fixed_len;
+    a.causal_extra = causal_extra;
+    a.max_kv_len = max_kv_len;
+    a.n_splits = n_splits;
+    a.out = out;
+    a.out_lse = out_lse;
+    a.err = d_err;
+    const size_t rows = (size_t)k->n_seq * n_q * n_heads;
+    if (n_splits > 1) {
+        a.part_o = static_cast<float *>(workspace);
+        a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align256((size_t)n_splits * rows * k->head_dim * sizeof(float)));
+    }
+    cudaError_t le;
+    if (kvq::decode_tc_supported(a)) le = kvq::launch_decode_tc(a, q_dtype, cs);
+    else le = kvq::launch_decode_simt(a, q_dtype, cs);
+    kvq_status st;
+    if ((st = cuda_status(le, "decode launch")) != KVQ_OK) return st;
+    if (n_splits > 1)
+        return cuda_status(kvq::launch_merge(a.part_o, a.part_lse, n_splits, (int)rows, k->head_dim, out, out_lse, cs),
+                           "merge launch");
+    return KVQ_OK;
+}
+
+kvq_status kvq::check_cache_args(const kvq_cache *c, const char *name) { return check_cache(c, name); }
+
 extern "C" {
 
 int32_t kvq_row_bytes(int32_t codec, int32_t head_dim)
@@ -248,39 +306,8 @@ kvq_status kvq_decode_attention(const kvq_cache *k, const kvq_cache *v, const vo
         return fail(KVQ_EINVAL, "decode: workspace must be 256-byte aligned");
     if (s > 65535) return fail(KVQ_EINVAL, "decode: too many splits");
     if (k->n_seq > 65535 || k->n_kv_heads > 65535) return fail(KVQ_EUNSUPPORTED, "decode: grid too large");
-
-    kvq::DecodeArgs a{};
-    a.k = plane_of(k);
-    a.v = plane_of(v);
-    a.q = q;
-    a.n_seq = k->n_seq;
-    a.n_kv_heads = k->n_kv_heads;
-    a.n_heads = n_heads;
-    a.n_q = n_q;
-    a.head_dim = k->head_dim;
-    a.capacity = k->capacity;
-    a.scale_log2 = softmax_scale * kvq::kLog2e;
-    a.kv_len = d_kv_len;
-    a.max_kv_len = max_kv_len;
-    a.n_splits = s;
-    a.out = out;
-    a.out_lse = out_lse;
-    a.err = d_err;
-    const size_t rows = (size_t)k->n_seq * n_q * n_heads;
-    if (s > 1) {
-        a.part_o = static_cast<float *>(workspace);
-        a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align256((size_t)s * rows * k->head_dim * sizeof(float)));
-    }
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t le;
-    if (kvq::decode_tc_supported(a)) le = kvq::launch_decode_tc(a, q_dtype, cs);
-    else le = kvq::launch_decode_simt(a, q_dtype, cs);
-    if ((st = cuda_status(le, "decode launch")) != KVQ_OK) return st;
-    if (s > 1)
-        return cuda_status(kvq::launch_merge(a.part_o, a.part_lse, s, (int)rows, k->head_dim, out, out_lse, cs),
-                           "merge launch");
-    return KVQ_OK;
+    return kvq::decode_checked(k, v, q, q_dtype, n_q, n_heads, softmax_scale, d_kv_len, -1, 0, max_kv_len, s, out,
+                               out_lse, workspace, d_err, static_cast<cudaStream_t>(stream));
 }
 
 kvq_status kvq_merge_splits(const float *part_o, const float *part_lse, int32_t n_splits, int32_t rows,

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
     // no early trigger: a dependent merge launch starts once this grid ends
     pdl_wait();
 
-    int len = a.kv_len[s];
+    int len = a.fixed_len >= 0 ? a.fixed_len : a.kv_len[s];
     if (len < 0 || len > a.max_kv_len) {
         if (threadIdx.x == 0 && split == 0 && kh == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
         len = len < 0 ? 0 : a.max_kv_len;
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(DecodeArgs
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             const int i = (rb0 + r) / G;
-            nvis[r] = (r < nr) ? len - a.n_q + i + 1 : 0;
+            nvis[r] = (r < nr) ? len + a.causal_extra - a.n_q + i + 1 : 0;
         }
         float m[RB], l[RB], o[RB][VPL];
 #pragma unroll

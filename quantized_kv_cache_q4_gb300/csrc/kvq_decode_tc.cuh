@@ -200,7 +200,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         }
     }
 
-    int len = a.kv_len[s];
+    int len = a.fixed_len >= 0 ? a.fixed_len : a.kv_len[s];
     if (len < 0 || len > a.max_kv_len) {
         if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0 && a.err) atomicOr(a.err, KVQ_ERR_KV_LEN);
         len = len < 0 ? 0 : a.max_kv_len;
@@ -209,7 +209,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
     split_range(len, a.n_splits, split, lo, hi);
     // no row of this CTA sees past its last query token's keys (with one row
     // block the last row is the last query token, which sees them all)
-    if (a.n_row_blocks > 1) hi = max(lo, min(hi, len - a.n_q + (r0 + R - 1) / G + 1));
+    if (a.n_row_blocks > 1) hi = max(lo, min(hi, len + a.causal_extra - a.n_q + (r0 + R - 1) / G + 1));
     const int n_tiles = (int)ceil_div(hi - lo, kTile);
     const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
     const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
@@ -234,7 +234,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int r = nt * 8 + 2 * tig + c;
-            nv[nt][c] = r < R ? len - a.n_q + (r0 + r) / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
+            nv[nt][c] = r < R ? len + a.causal_extra - a.n_q + (r0 + r) / G + 1 : 0x7FFFFFFF;   // padding rows: no mask
             nv_min = min(nv_min, nv[nt][c]);
         }
     const float sl2 = a.scale_log2;

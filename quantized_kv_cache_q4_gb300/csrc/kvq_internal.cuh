@@ -111,6 +111,13 @@ struct DecodeArgs {
     float *part_o, *part_lse;   // [n_splits][rows][D], [n_splits][rows] (n_splits > 1)
     int32_t *err;
     int n_row_blocks = 1;       // tensor-core kernel: CTAs per (split, kv head), 32 query rows each
+    // Key ranges that are one part of a longer context (host-tier streaming):
+    // fixed_len >= 0 replaces kv_len[s] (one sequence, length known on the
+    // host), and query token i sees len + causal_extra - n_q + i + 1 keys of
+    // the range (capped by len): causal_extra counts the context's keys after
+    // the range.
+    int fixed_len = -1;
+    int causal_extra = 0;
 };
 
 // Query rows per kv head the tensor-core kernel gives one CTA, and the blocks
@@ -159,6 +166,22 @@ inline int per_device(PerDevice &pd, int dev, F compute)
 
 // Set the message kvq_last_error() returns on the calling thread.
 void set_last_error(const char *msg);
+// Set it printf-style and return st.
+kvq_status fail_msg(kvq_status st, const char *fmt, ...);
+// The argument checks every cache goes through (KVQ_OK or the failure, with
+// the message set).
+kvq_status check_cache_args(const kvq_cache *c, const char *name);
+// The split count kvq_decode_attention uses (n_splits = 0: its default).
+int resolve_decode_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q, int32_t max_kv_len,
+                          int32_t n_splits);
+// Decode attention with validated arguments and a resolved split count:
+// launches the decode kernel and, with n_splits > 1, the merge into out/out_lse
+// (the partials in workspace).  fixed_len >= 0 gives one sequence's key count
+// on the host instead of d_kv_len; causal_extra is DecodeArgs::causal_extra.
+kvq_status decode_checked(const kvq_cache *k, const kvq_cache *v, const void *q, int q_dtype, int n_q, int n_heads,
+                          float softmax_scale, const int32_t *d_kv_len, int fixed_len, int causal_extra,
+                          int max_kv_len, int n_splits, float *out, float *out_lse, void *workspace, int32_t *d_err,
+                          cudaStream_t cs);
 
 cudaError_t launch_append(const AppendArgs &a, bool src_f16, cudaStream_t st);
 cudaError_t launch_decode_simt(const DecodeArgs &a, int q_dtype, cudaStream_t st);

@@ -148,3 +148,49 @@ def test_status_strings():
     for s in range(5):
         assert kvq.kvq_status_string(s)
     assert kvq.kvq_status_string(99) == "unknown status"
+
+
+def _tiered(k, v, kd=None, vd=None, n_res=0, q=4096, n_q=1, n_heads=24, kv_len=1000, page=256, slots=2,
+            ring=1 << 20, ring_bytes=1 << 30, out=4096, ws=1 << 20, ws_bytes=1 << 30):
+    ref = lambda c: ctypes.byref(c) if c is not None else None   # noqa: E731
+    return kvq._lib.kvq_decode_attention_tiered(ref(k), ref(v), ref(kd), ref(vd), n_res, q, kvq.KVQ_F16, n_q,
+                                                n_heads, 0.0625, kv_len, page, slots, ring, ring_bytes, out, None,
+                                                ws, ws_bytes, None, None)
+
+
+def test_tiered_rejects_bad_arguments():
+    k, v = _fake_cache(), _fake_cache()
+    assert _tiered(_fake_cache(n_seq=2), _fake_cache(n_seq=2)) == kvq.KVQ_EUNSUPPORTED   # one sequence only
+    assert _tiered(k, _fake_cache(head_dim=128)) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, n_heads=22) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, n_q=0) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, kv_len=0) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, kv_len=1025) == kvq.KVQ_EINVAL                 # beyond the host capacity
+    assert _tiered(k, v, page=100) == kvq.KVQ_EINVAL                    # not a multiple of 64
+    assert _tiered(k, v, slots=0) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, n_res=10) == kvq.KVQ_EINVAL                    # resident part without device caches
+    assert _tiered(k, v, n_res=1001) == kvq.KVQ_EINVAL                  # more resident keys than keys
+    assert _tiered(k, v, kd=_fake_cache(codec=kvq.KVQ_CODEC_Q8_0), vd=_fake_cache(), n_res=10) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, kd=_fake_cache(capacity=64), vd=_fake_cache(capacity=64), n_res=100) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, q=None) == kvq.KVQ_EINVAL
+    assert _tiered(k, v, out=None) == kvq.KVQ_EINVAL
+    need = kvq.kvq_tiered_ring_bytes(k, v, 256, 2)
+    assert _tiered(k, v, ring_bytes=need - 1) == kvq.KVQ_EWORKSPACE
+    assert _tiered(k, v, ring=None) == kvq.KVQ_EWORKSPACE
+    assert _tiered(k, v, ring=(1 << 20) + 16) == kvq.KVQ_EINVAL          # misaligned
+    assert _tiered(k, v, ws_bytes=64) == kvq.KVQ_EWORKSPACE
+    assert _tiered(k, v, ws=(1 << 20) + 16) == kvq.KVQ_EINVAL
+    assert kvq.kvq_last_error()
+
+
+def test_tiered_sizes():
+    k, v = _fake_cache(), _fake_cache(codec=kvq.KVQ_CODEC_Q8_0)
+    # a slot holds every kv head's page of each plane, each plane 256-byte aligned
+    rows = 4 * 256
+    slot = rows * 128 + rows * 8 + rows * 256 + rows * 16
+    assert kvq.kvq_tiered_ring_bytes(k, v, 256, 3) == 3 * slot
+    assert kvq.kvq_tiered_ring_bytes(k, v, 0, 3) == 0
+    # per-part partials (resident part + ceil(900 / 256) = 4 pages) and split scratch
+    ws = kvq.kvq_tiered_workspace_bytes(k, v, None, None, 24, 3, 1000, 100, 256)
+    assert ws >= 5 * 3 * 24 * (256 + 1) * 4
+    assert kvq.kvq_tiered_workspace_bytes(k, v, None, None, 22, 3, 1000, 100, 256) == 0
