@@ -128,10 +128,14 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t w, int e)
 // k-positions of one k-step, so of one K group); the CPG chunks of a group sit
 // in consecutive lanes, whose shuffle sum gives minus the group's bias term
 // sum_d bias(d) q(d) (bias 1032 at even, 1152 at odd d for Q4_G64; 1152 for
-// q8_0) in kb_s[group][row].
+// q8_0) in kb_s[group][row].  An fp32 query is split into fp16 parts,
+// value = hi + lo: hi goes to qp, lo (the fp32 remainder rounded to fp16) to
+// qp_lo in the same layout, and the bias terms cover hi + lo; the K product
+// then takes one MMA per part, so the query keeps about 22 bits instead of 11.
 template <int KC, int D, int ROWS, int NTH, typename QT>
-__device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb_s, int R, bool ok)
+__device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, uint8_t *qp_lo, float *kb_s, int R, bool ok)
 {
+    constexpr bool SPLIT = sizeof(QT) == 4;
     constexpr int CPR = D / 8;                     // chunks per row
     constexpr int CPG = (is_fp4(KC) ? 64 : group_size(KC)) / 8;   // chunks per K accumulation group
     for (int ci = threadIdx.x; ci < ROWS * CPR; ci += NTH) {   // whole warps per step
@@ -144,23 +148,31 @@ __device__ __forceinline__ void prep_query(const QT *qst, uint8_t *qp, float *kb
             x[j] = 0.0f;
             if (n < R && ok) {
                 if constexpr (sizeof(QT) == 2) x[j] = __half2float(qst[n * D + d]);
-                else x[j] = __half2float(__float2half_rn(qst[n * D + d]));
+                else x[j] = qst[n * D + d];
             }
             if constexpr (is_q4(KC))
                 if (d & 1) x[j] *= 0.0625f;
         }
-        uint32_t hw[4];
+        uint32_t hw[4], lw[4];
         float b = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             hw[j] = pack_f16x2(x[2 * j], x[2 * j + 1]);
-            const float2 hf = __half22float2(u32_as_h2(hw[j]));
+            float2 hf = __half22float2(u32_as_h2(hw[j]));
+            if constexpr (SPLIT) {
+                lw[j] = pack_f16x2(x[2 * j] - hf.x, x[2 * j + 1] - hf.y);   // exact fp32 remainders, rounded
+                const float2 lf = __half22float2(u32_as_h2(lw[j]));
+                hf.x += lf.x;
+                hf.y += lf.y;
+            }
             // Q4_G64: j-th pair is (d, d + 4) with d's parity that of the k-step
             const int kg = 8 * c + 2 * j;
             const bool even = is_q4(KC) && ((kpos_to_d<KC>(kg >> 4, kg & 15) & 1) == 0);
             if constexpr (!is_fp4(KC)) b = fmaf(even ? 1032.0f : 1152.0f, hf.x + hf.y, b);
         }
         *reinterpret_cast<uint4 *>(qp + qp_chunk_off<D>(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if constexpr (SPLIT)
+            *reinterpret_cast<uint4 *>(qp_lo + qp_chunk_off<D>(n, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 #pragma unroll
         for (int off = 1; off < CPG; off <<= 1) b += __shfl_xor_sync(0xffffffffu, b, off);
         if (c % CPG == 0) kb_s[(c / CPG) * ROWS + n] = -b;

@@ -80,7 +80,10 @@ struct TcCfg {
     // (q8_0 K and V: 34 KB a stage)
     static constexpr int NS = STAGE <= 27 * 1024 ? 3 : 2;
     static constexpr int QP_OFF = NS * STAGE;                     // fp16 [ROWS][D], permuted, swizzled
-    static constexpr int KB_OFF = QP_OFF + ROWS * D * 2;          // fp32 [NGK][ROWS]: minus the K bias terms
+    // an fp32 query also keeps its low fp16 part (same layout)
+    static constexpr bool QLO = sizeof(QT) == 4;
+    static constexpr int QPL_OFF = QP_OFF + ROWS * D * 2;
+    static constexpr int KB_OFF = QPL_OFF + (QLO ? ROWS * D * 2 : 0);   // fp32 [NGK][ROWS]: minus the K bias terms
     // the query rows as given are only read before the first tile, the score
     // tiles and the maxima only after it: they share one region
     static constexpr int U_OFF = KB_OFF + align_up(ROWS * NGK * 4, 16);
@@ -224,7 +227,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
 
     // the query rows, permuted and swizzled, and the K bias terms
     if (!mbar_wait(bar_q, 0)) s_timeout = 1;
-    prep_query<KC, D, C::ROWS, kT>(reinterpret_cast<const QT *>(smem + C::QST_OFF), qp, kb_s, R, !s_timeout);
+    prep_query<KC, D, C::ROWS, kT>(reinterpret_cast<const QT *>(smem + C::QST_OFF), qp, smem + C::QPL_OFF, kb_s, R,
+                                   !s_timeout);
     __syncthreads();
 
     int nv[NT][2];
@@ -271,9 +275,11 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
         const int ca = V8 ? MTW * warp + 2 * u : cw, cb = V8 ? (MTW >= 2 ? ca + 1 : ca) : cw1;
         voff[u] = VG::chunk_addr(C::V_OFF, (lane & 7) + 8 * (lane >> 4), ((lane >> 3) & 1) ? cb : ca);
     }
-    const uint32_t qp_base = smem_u32(qp);
+    const uint32_t qp_base = smem_u32(qp), qpl_base = smem_u32(smem + C::QPL_OFF);
     // with one n-tile the query's B fragments fit in registers for the whole CTA
-    constexpr bool QREG = (NT == 1);
+    // (an fp16 query; the two parts of an fp32 one are read from shared memory)
+    constexpr bool QLO = C::QLO;
+    constexpr bool QREG = (NT == 1) && !QLO;
     constexpr int KSTEPS = D / 16;
     uint32_t qf[QREG ? KSTEPS : 1][2];
     if constexpr (QREG) {
@@ -412,6 +418,20 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, co
                         } else {
                             mma16816(cg[2 * np], a0, a1, a2, a3, b00, b01);
                             if (2 * np + 1 < NT) mma16816(cg[2 * np + 1], a0, a1, a2, a3, b10, b11);
+                        }
+                        if constexpr (QLO) {
+                            // the low part of an fp32 query, into the same accumulators
+                            if (2 * np + 1 < NT) {
+                                const int qrow = (2 * np + (lane >> 4)) * 8 + (lane & 7);
+                                ldsm_x4(qpl_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01, b10,
+                                        b11);
+                                mma16816(cg[2 * np], a0, a1, a2, a3, b00, b01);
+                                mma16816(cg[2 * np + 1], a0, a1, a2, a3, b10, b11);
+                            } else {
+                                const int qrow = 2 * np * 8 + (lane & 7);
+                                ldsm_x2(qpl_base + qp_chunk_off<D>(qrow, 2 * ks + ((lane >> 3) & 1)), b00, b01);
+                                mma16816(cg[2 * np], a0, a1, a2, a3, b00, b01);
+                            }
                         }
                     }
                 }

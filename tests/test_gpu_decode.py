@@ -31,6 +31,23 @@ def test_workload_default_splits(cfg):
     check_close(o, o_ref, lse, lse_ref)
 
 
+@pytest.mark.parametrize("kc,vc", [(kvq.KVQ_CODEC_Q4_G64, kvq.KVQ_CODEC_Q4_G64), (kvq.KVQ_CODEC_Q8_0, kvq.KVQ_CODEC_Q4_G64),
+                                   (kvq.KVQ_CODEC_Q4_G32, kvq.KVQ_CODEC_Q8_0), (kvq.KVQ_CODEC_NVFP4, kvq.KVQ_CODEC_NVFP4)])
+@pytest.mark.parametrize("D,G,n_new", [(128, 6, 3), (256, 6, 1), (64, 8, 4)])
+def test_fp32_query_with_outlier_keys(kc, vc, D, G, n_new):
+    """An fp32 query reaches the tensor cores as two fp16 parts (hi + lo), so
+    large keys (outliers x8) do not magnify its rounding: rounded to one fp16
+    part, this shape missed the bar by 1.5x (max-abs 3.0e-3 at head_dim 128)."""
+    wl = workloads.custom(n_seq=1, n_heads=4 * G, n_kv_heads=4, head_dim=D, cached=(4997,), n_new=n_new, k_codec=kc,
+                          v_codec=vc, src_dtype="f16", q_dtype="f32", dist="outliers", seed=71 + kc + D + G)
+    k, v, ko, vo = _both(wl)
+    o_ref, lse_ref = oracle.decode_attention(ko, vo, wl.q, wl.kv_len, wl.spec.scale)
+    for n_splits in (0, 1):
+        o, lse, err = run_decode(wl, k, v, n_splits=n_splits)
+        assert err == 0
+        check_close(o, o_ref, lse, lse_ref)
+
+
 def test_long196k_explicit_splits():
     """The 196,608-key workload at full size with 64 and 256 splits of the key
     range (besides the default count), each merged by log-sum-exp."""
