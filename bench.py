@@ -64,8 +64,8 @@ def _peaks():
 
 # The sources of the kernels the committed captures profile (the Q4_G64 decode
 # and the merge) and of their launch (split policy, tensor maps).
-_PROFILED_SOURCES = ("kvq_api.cu", "kvq_decode_tc.cu", "kvq_decode_tc.cuh", "kvq_internal.cuh", "kvq_merge.cu",
-                     "kvq_ptx.cuh", "kvq_tensor_map.cu")
+_PROFILED_SOURCES = ("kvq_api.cu", "kvq_decode_common.cuh", "kvq_decode_tc.cu", "kvq_decode_tc.cuh",
+                     "kvq_internal.cuh", "kvq_merge.cu", "kvq_ptx.cuh", "kvq_tensor_map.cu")
 
 
 def _kernel_hash() -> str:
@@ -505,7 +505,7 @@ def attention_summary(sess, attn_ms, attn_eager_ms, step_ms, clocks, peak):
     return {"workload": sp.name, "kv_bytes_per_step": kv, "total_kv_tokens": int(sess.wl.kv_len.sum()),
             "n_splits": sess.n_splits_eff, "attention_us": round(attn_ms * 1e3, 3),
             "attention_us_eager_call": round(attn_eager_ms * 1e3, 3), "attention_gbs": round(gbs, 2),
-            "frac": round(gbs / peak, 4), "step_us": round(step_ms * 1e3, 3),
+            "frac": round(gbs / peak, 4), "traffic": _traffic(sp.name), "step_us": round(step_ms * 1e3, 3),
             "step_gbs": round(kv / (step_ms * 1e-3) / 1e9, 2),
             "us_per_token": round(step_ms * 1e3 / (sp.n_seq * sp.n_q), 4), "clocks": clocks,
             "l2": f"{sess.n_copies} rotating cache copies, steps replayed from CUDA graphs"}
