@@ -601,6 +601,8 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
             also[wl2.spec.name] = attention_summary(s2, attn2, eager2, ms2, clocks2, peak)
             del s2
             torch.cuda.empty_cache()
+        also["long196k_host_tier"] = host_tier_summary(args, dev, peak)
+        torch.cuda.empty_cache()
         res["also"] = also
     return res
 
@@ -608,6 +610,60 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
 # workloads measured beside the main one: 196,608 keys, the 16-sequence MTP
 # verify batch, the mixed q8_0-K / Q4_G64-V pair at 65,536 keys
 ALSO_CONFIGS = (3, 4, 2)
+
+
+def host_tier_summary(args, dev, peak, resident_frac=0.5, page_tokens=8192, n_slots=4):
+    """The 196,608-key workload with its cache in pinned host memory: the first
+    half resident on the device, the rest streamed through a ring of n_slots
+    pages (kvq_decode_attention_tiered).  Timed with CUDA events around calls on
+    the caller's stream (the page copies run on the library's copy stream,
+    joined to it)."""
+    import torch
+    import quantized_kv_cache_q4_gb300 as kvq
+    wl = workloads.make(workloads.spec(3))
+    sp = wl.spec
+    S, Hk, D, H, nq = sp.n_seq, sp.n_kv_heads, sp.head_dim, sp.n_heads, sp.n_q
+    kv_len = int(wl.kv_len[0])
+    k = kvq.KVCache(sp.k_codec, S, Hk, D, wl.capacity, device=dev)
+    v = kvq.KVCache(sp.v_codec, S, Hk, D, wl.capacity, device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    src = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)   # noqa: E731
+    kvq.kvq_quantize_append(k, v, src(wl.k_prefill[0][None]), src(wl.v_prefill[0][None]), int(wl.cached_len[0]), zero)
+    kvq.kvq_quantize_append(k, v, src(wl.k_new), src(wl.v_new), nq, src(wl.cached_len))
+    torch.cuda.synchronize()
+    kh, vh = k.to_host(), v.to_host()
+    n_res = int(kv_len * resident_frac) // 64 * 64
+    ring = kvq.alloc_workspace(kvq.kvq_tiered_ring_bytes(kh, vh, page_tokens, n_slots), dev)
+    ws = kvq.alloc_workspace(kvq.kvq_tiered_workspace_bytes(kh, vh, k, v, H, nq, kv_len, n_res, page_tokens), dev)
+    q = src(wl.q)
+    out = torch.empty((S, nq, H, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((S, nq, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        kvq.kvq_decode_attention_tiered(kh, vh, k, v, n_res, q, nq, H, sp.scale, kv_len, page_tokens, n_slots, ring,
+                                        out, lse, ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            call()
+    stream.synchronize()
+    reps = max(5, args.steps // 4)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / reps
+    kv = workloads.kv_bytes_per_token(sp) * kv_len
+    streamed = workloads.kv_bytes_per_token(sp) * (kv_len - n_res)
+    return {"workload": "long196k, cache in pinned host memory", "resident_tokens": n_res,
+            "streamed_tokens": kv_len - n_res, "page_tokens": page_tokens, "ring_slots": n_slots,
+            "attention_us": round(ms * 1e3, 3), "attention_gbs": round(kv / (ms * 1e-3) / 1e9, 2),
+            "frac": round(kv / (ms * 1e-3) / 1e9 / peak, 4),
+            "host_to_device_gbs": round(streamed / (ms * 1e-3) / 1e9, 2),
+            "timing": f"events around {reps} eager calls on the caller's stream"}
 
 
 def main():

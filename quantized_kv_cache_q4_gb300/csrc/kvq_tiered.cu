@@ -11,10 +11,11 @@
 // library's decode kernels into a partial (o, lse) normalised over the part,
 // and the partials are merged by the merge kernel.  A page is copied from the
 // host planes into ring slot p % n_slots by cudaMemcpy2DAsync (one call per
-// plane, all kv heads at once) on a copy stream of the library's own; the
-// copy of page p waits for the decode of page p - n_slots (which read that
-// slot), the decode of page p waits for its copy, so copies of later pages
-// run while earlier ones are decoded.  One sequence (a single serving slot).
+// plane, all kv heads at once) on copy streams of the library's own (pages
+// round-robin over them); the copy of page p waits for the decode of page
+// p - n_slots (which read that slot), the decode of page p waits for its copy,
+// so copies of later pages run while earlier ones are decoded.  One sequence
+// (a single serving slot).
 #include <cmath>
 #include <cstring>
 
@@ -74,13 +75,18 @@ size_t inner_ws(const kvq_cache *k_dev, const kvq_cache *v_dev, const kvq_cache 
     return need > p ? need : p;
 }
 
-// The library's copy stream on the current device (created once per device).
+// The library's copy streams on the current device (created once per device);
+// consecutive pages go to different streams.  One: on GB300 a page copy from
+// pinned host memory runs at ~160 GB/s whether 1, 2, 4 or 8 streams share
+// the pages (measured), so more streams only add events.
+constexpr int kCopyStreams = 1;
+
 struct CopyStreams {
     std::mutex mu;
-    cudaStream_t s[kvq::PerDevice::kMaxDevices] = {};
+    cudaStream_t s[kvq::PerDevice::kMaxDevices][kCopyStreams] = {};
 };
 
-cudaError_t copy_stream(cudaStream_t *out)
+cudaError_t copy_streams(cudaStream_t (&out)[kCopyStreams])
 {
     static CopyStreams cs;
     int dev = 0;
@@ -88,14 +94,16 @@ cudaError_t copy_stream(cudaStream_t *out)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kvq::PerDevice::kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(cs.mu);
-    if (!cs.s[dev]) {
-        e = cudaStreamCreateWithFlags(&cs.s[dev], cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            cs.s[dev] = nullptr;
-            return e;
+    for (int i = 0; i < kCopyStreams; ++i) {
+        if (!cs.s[dev][i]) {
+            e = cudaStreamCreateWithFlags(&cs.s[dev][i], cudaStreamNonBlocking);
+            if (e != cudaSuccess) {
+                cs.s[dev][i] = nullptr;
+                return e;
+            }
         }
+        out[i] = cs.s[dev][i];
     }
-    *out = cs.s[dev];
     return cudaSuccess;
 }
 
@@ -216,8 +224,8 @@ kvq_status kvq_decode_attention_tiered(const kvq_cache *k_host, const kvq_cache 
         if ((st = decode_part(k_dev, v_dev, n_resident, n_resident, idx++)) != KVQ_OK) return st;
     }
     if (n_pages > 0) {
-        cudaStream_t cp = nullptr;
-        cudaError_t e = copy_stream(&cp);
+        cudaStream_t cps[kCopyStreams] = {};
+        cudaError_t e = copy_streams(cps);
         if (e != cudaSuccess) return kvq::fail_msg(KVQ_ECUDA, "tiered: copy stream: %s", cudaGetErrorString(e));
         const RingLayout rl = ring_layout(k_host, v_host, page_tokens);
         const int kv = k_host->n_kv_heads, cap = k_host->capacity;
@@ -242,10 +250,12 @@ kvq_status kvq_decode_attention_tiered(const kvq_cache *k_host, const kvq_cache 
         for (int i = 0; i < n_pages + n_slots; ++i)
             if ((e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e, "event");
         cudaEvent_t *copied = ev, *freed = ev + n_pages;
-        if ((e = cudaEventRecord(start, cs)) != cudaSuccess || (e = cudaStreamWaitEvent(cp, start, 0)) != cudaSuccess)
-            return cuda_fail(e, "stream join");
+        if ((e = cudaEventRecord(start, cs)) != cudaSuccess) return cuda_fail(e, "stream join");
+        for (int i = 0; i < kCopyStreams && i < n_pages; ++i)
+            if ((e = cudaStreamWaitEvent(cps[i], start, 0)) != cudaSuccess) return cuda_fail(e, "stream join");
         for (int p = 0; p < n_pages; ++p) {
             const int slot = p % n_slots;
+            cudaStream_t cp = cps[p % kCopyStreams];
             const int t0 = n_resident + p * page_tokens;
             const int len = kv_len - t0 < page_tokens ? kv_len - t0 : page_tokens;
             uint8_t *base = static_cast<uint8_t *>(ring) + (size_t)slot * rl.slot;
