@@ -49,7 +49,7 @@ typedef enum kvq_status {
 } kvq_status;
 
 /* Codecs of a cache plane.
- * KVQ_CODEC_Q4_G64 -- signed INT4 codes with one FP16 scale per 64 values,
+ * KVQ_CODEC_Q4_G64 -- 4-bit signed codes, one fp16 scale per group of 64 values,
  *   4.25 bits per value (den_llama.cpp, "What this fork is", quantized KV
  *   cache bullet; "build3 (working engine) -- additions", Q4_G64 row).
  *   Per group: scale = fp16_rne(absmax / 7) (fp32 quotient, saturated to

@@ -8,7 +8,7 @@
  * calls it.
  *
  * What it follows:
- *   - The Q4_G64 codec: signed INT4 values with one FP16 scale per 64 values,
+ *   - The Q4_G64 codec: 4-bit signed codes, an fp16 scale for each group of 64 values,
  *     4.25 bits per value (den_llama.cpp, "What this fork is", quantized KV
  *     cache bullet; "build3 (working engine) -- additions" table, Q4_G64 row,
  *     whose footnote says the CUDA quantizer is byte-identical to a CPU

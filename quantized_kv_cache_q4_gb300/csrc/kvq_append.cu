@@ -1,8 +1,8 @@
 // kvq_append.cu -- quantize-on-append: new K/V rows are quantized to Q4_G64,
 // Q4_G32, q8_0 or NVFP4 and written at their cache positions (den_llama.cpp,
 // "What's in the fork": the set-rows / cpy-utils quantize path of the Q4_G64
-// codec; the codec itself in "What this fork is": signed INT4 + one FP16
-// scale per 64 values; the NVFP4 KV type of the same section, read as
+// codec; the codec itself in "What this fork is": 4-bit signed codes sharing
+// an fp16 scale per 64-value group; the NVFP4 KV type of the same section, read as
 // NVIDIA's published NVFP4).
 //
 // One warp quantizes one (plane, sequence, new token, kv head) row.  Lane l

@@ -9,7 +9,7 @@
 // value times an E4M3 scale has at most 6 significant bits), so they need no
 // bias, offset or per-group scaling of the accumulators.
 // (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
-// this fork is": signed INT4 + one FP16 scale per 64 values; "Results": MTP
+// this fork is": the 4-bit code with an fp16 scale per 64-value group; "Results": MTP
 // n-max 2, i.e. 1 + 2 query tokens per sequence).
 //
 // Per (sequence, kv head, split) the query rows of the kv head attend to the

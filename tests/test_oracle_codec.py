@@ -1,6 +1,6 @@
 """Pins the oracle's Q4_G64, Q4_G32 and q8_0 codecs.
 
-What fixes the codec: signed INT4 with one FP16 scale per 64 values, exactly
+What fixes the codec: 4-bit signed codes, one fp16 scale for each 64-value group, exactly
 4.25 bits/value (den_llama.cpp, "What this fork is", quantized KV cache
 bullet); the q8_0-style K of the mixed pair (den_llama.cpp, "Build3 (working
 engine)" command block); the pages' "q4_0" V, read as the Q4_G64 rule with
