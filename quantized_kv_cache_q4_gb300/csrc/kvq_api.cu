@@ -86,10 +86,16 @@ int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int3
 {
     if (n_splits > 0) return n_splits;
     const int rows = n_q * (n_heads / k->n_kv_heads);
-    // one CTA per (sequence, kv head, block of query rows) and split
-    const int64_t units = (int64_t)k->n_seq * k->n_kv_heads * (k->head_dim <= 256 ? kvq::tc_row_blocks(rows) : 1);
-    // CTAs of the decode kernel an SM holds (3 where the occupancy is unknown)
-    int per_sm = kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, rows);
+    // one CTA per (sequence, kv head, block of query rows) and split; prompt
+    // chunks the tcgen05 kernel takes come in blocks of 128 rows
+    const bool umma = kvq::prefill_umma_shape(k->codec, v->codec, k->head_dim, rows) &&
+                      kvq::prefill_umma_ctas_per_sm(k->codec, v->codec, k->head_dim) > 0;
+    const int64_t blocks = umma ? kvq::ceil_div(rows, kvq::kUmmaRowsPerCta)
+                                : (k->head_dim <= 256 ? kvq::tc_row_blocks(rows) : 1);
+    const int64_t units = (int64_t)k->n_seq * k->n_kv_heads * blocks;
+    // CTAs of the kernel an SM holds (3 where the occupancy is unknown)
+    int per_sm = umma ? kvq::prefill_umma_ctas_per_sm(k->codec, v->codec, k->head_dim)
+                      : kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, rows);
     if (per_sm <= 0) per_sm = 3;
     int64_t target;
     if (k->n_seq == 1) {

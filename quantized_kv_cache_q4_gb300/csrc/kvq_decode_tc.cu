@@ -26,6 +26,7 @@ int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_h
 
 cudaError_t launch_decode_tc(const DecodeArgs &args, int q_dtype, cudaStream_t st)
 {
+    if (prefill_umma_takes(args, q_dtype)) return launch_prefill_umma(args, st);
     DecodeArgs a = args;
     a.n_row_blocks = tc_row_blocks(a.n_q * (a.n_heads / a.n_kv_heads));
     if (a.v.codec == KVQ_CODEC_Q4_G64) return launch_for_v<KVQ_CODEC_Q4_G64>(a, q_dtype, st);

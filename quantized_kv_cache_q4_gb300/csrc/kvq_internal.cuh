@@ -199,6 +199,16 @@ cudaError_t launch_decode_tc_q8v(const DecodeArgs &a, int q_dtype, cudaStream_t 
 int decode_tc_q8v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 cudaError_t launch_decode_tc_fp4v(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 int decode_tc_fp4v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
+// Prompt-chunk path on the fifth-generation tensor cores (tcgen05): blocks of
+// 128 query rows per CTA, Q4_G64 K and V, head_dim 64/128/256,
+// fp16 queries.  prefill_umma_shape: the shapes it is meant for (rows per kv
+// head at least kUmmaMinRows); prefill_umma_takes: it runs these arguments.
+constexpr int kUmmaMinRows = 64;
+constexpr int kUmmaRowsPerCta = 128;
+bool prefill_umma_shape(int k_codec, int v_codec, int head_dim, int rows_per_kv_head);
+bool prefill_umma_takes(const DecodeArgs &a, int q_dtype);
+int prefill_umma_ctas_per_sm(int k_codec, int v_codec, int head_dim);
+cudaError_t launch_prefill_umma(const DecodeArgs &a, cudaStream_t st);
 cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int rows, int head_dim,
                          float *out, float *out_lse, cudaStream_t st);
 cudaError_t launch_dequant(const Plane &p, int64_t n_rows, int head_dim, float *out, cudaStream_t st);
