@@ -9,26 +9,25 @@
 // V are Q4_G64.  Per 64-token tile:
 //  * TMA has brought the tile's K and V codes (swizzled 2D boxes) and scales
 //    (bulk copies) into a 3-stage ring (the decode kernel's tile format).
-//  * All 8 warps turn the K codes into exact fp16 integers (q at even
-//    head_dim indices, 16 q at odd ones; the query is stored with its odd
-//    indices divided by 16), laid out as the K-major B operand of S = Q K^T
-//    (128-byte swizzled rows of 64 values), and the tile's scales into fp32.
-//  * One thread issues S_g = Q_g K_g^T for each 64-value group g (M = 128
-//    rows, N = 64 tokens, K = 64) into its own 64 tensor-memory columns, so
-//    the fp16 group scales are applied in fp32 afterwards, as the decode
-//    kernel does: no rounding of K beyond the codes themselves.
-//  * The warps turn the V codes into exact fp16 integers in the same buffer
-//    (S = Q K^T has finished reading it) -- in these bytes the MN-major B
-//    operand of O = P V -- and compute the softmax: each row is read back by
+//  * All 8 warps turn the K tile into two fp16 operands whose sum is K / 16
+//    exactly: each fp16 group scale s is cut into s_hi (its top 7 significant
+//    bits) and s_lo = s - s_hi (at most 4), so that q * s_hi / 16 and
+//    q * s_lo / 16 are both exact in fp16 for any signed nibble q (the 1/16
+//    keeps every product finite for any fp16 scale).  They are laid out as
+//    K-major B operands: 128-byte swizzled rows of 64 values.
+//  * One thread issues S = Q K_hi^T + Q K_lo^T (M = 128 rows, N = 64
+//    tokens, K = head_dim) into 64 tensor-memory columns: the scores are
+//    those of the exact dequantized keys, accumulated in fp32.
+//  * The warps turn the V tile the same way into V_hi + V_lo in the same
+//    buffer (S has finished reading it) -- in these bytes the MN-major B
+//    operands of O = P V -- and compute the softmax: each row is read back by
 //    two threads (warps w and w + 4 share lane quarter w % 4; one takes tokens
 //    0-31, the other 32-63), whose maxima are combined through shared memory;
-//    x = sum_g s_K(t, g) S_g (log2 units); where a row's maximum grows, its O
-//    columns are rescaled in tensor memory.  P'_g = p * s_V(t, g) is rounded
-//    once to fp16 per V group (the decode kernel's rule: the largest weight of
-//    a row is then its scale exactly) into shared memory, the K-major A
-//    operands of O_g += P'_g V_g.
-//  * One thread issues O_g += P'_g V_g (M = 128, N = 64, K = 64 tokens) for
-//    each group into the group's 64 columns of O in tensor memory.
+//    where a row's maximum grows, its O columns are rescaled in tensor memory.
+//    p = 2^(s - m) (<= 1, the largest exactly 1) is rounded once to fp16 into
+//    shared memory, the K-major A operand of O += P V.
+//  * One thread issues O += P V_hi + P V_lo (M = 128, N = head_dim, K = 64
+//    tokens) into head_dim tensor-memory columns.
 // The tensor core and the CUDA cores take turns inside a CTA (no warp
 // specialisation yet); CTAs on other SMs overlap.  Within each 8-value group
 // the head_dim order is the one the nibble unpack delivers (value pairs
@@ -149,16 +148,15 @@ struct UmCfg {
     static constexpr int KC = KVQ_CODEC_Q4_G64, VC = KVQ_CODEC_Q4_G64;
     static constexpr int KRB = row_bytes(KC, D), VRB = row_bytes(VC, D);
     static constexpr int KSB = scale_row_bytes(KC, D), VSB = scale_row_bytes(VC, D);
-    static constexpr int NG = D / 64;                             // 64-value groups (= scale groups)
+    static constexpr int NG = D / 64;                             // 64-value blocks (= scale groups)
     // shared memory (from a 1024-aligned base)
     static constexpr int Q_OFF = 0;                               // [NG][128 rows][128 B]
     static constexpr int Q_BLOCK = kURows * 128;
-    static constexpr int X_OFF = Q_OFF + NG * Q_BLOCK;            // K, then V codes: [NG][64 tokens][128 B]
+    static constexpr int X_OFF = Q_OFF + NG * Q_BLOCK;            // K, then V: [hi, lo][NG][64 tokens][128 B]
     static constexpr int X_BLOCK = kUTile * 128;
-    static constexpr int P_OFF = X_OFF + NG * X_BLOCK;            // P'_g: [NG][128 rows][64 tokens] fp16
-    static constexpr int P_BLOCK = kURows * 128;
-    static constexpr int SF_OFF = P_OFF + NG * P_BLOCK;           // fp32 [2][NG][64]: K scales x log2 units, V scales
-    static constexpr int RING_OFF = align_up(SF_OFF + 2 * NG * kUTile * 4, 1024);
+    static constexpr int X_PART = NG * X_BLOCK;
+    static constexpr int P_OFF = X_OFF + 2 * X_PART;              // P: [128 rows][64 tokens] fp16
+    static constexpr int RING_OFF = P_OFF + kURows * 128;
     // ring stage: K codes, V codes (TMA boxes), K scales, V scales
     static constexpr int SK_OFF = 0;
     static constexpr int SV_OFF = align_up(kUTile * KRB, 1024);
@@ -170,11 +168,11 @@ struct UmCfg {
     static constexpr int BAR_OFF = RED_OFF + 2 * kURows * 4;      // full[NS], S done, O done
     static constexpr int TMEM_SLOT = BAR_OFF + (NS + 2) * 8;
     static constexpr int SMEM = TMEM_SLOT + 16 + 1024;            // + alignment slack
-    // tensor memory: S_g in columns [64 g, 64 g + 64), O in [64 NG, 64 NG + D)
-    static constexpr int S_COL = 0, O_COL = 64 * NG;
-    static constexpr int NCOL = 2 * D < 128 ? 128 : 2 * D;
+    // tensor memory: S in columns [0, 64), O in [64, 64 + D)
+    static constexpr int S_COL = 0, O_COL = 64;
+    static constexpr int NCOL = (64 + D) <= 128 ? 128 : (64 + D) <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC_S = umma_idesc(kURows, kUTile, 0);
-    static constexpr uint32_t IDESC_O = umma_idesc(kURows, 64, 1);
+    static constexpr uint32_t IDESC_O = umma_idesc(kURows, D, 1);
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -204,16 +202,28 @@ __device__ __forceinline__ void um_issue_tile(uint32_t st, uint32_t full, const 
     bulk_load_hint(st + C::SVS_OFF, vsc + row0 * C::VSB, kUTile * C::VSB, full, pol);
 }
 
-// One plane of a ring stage as exact fp16 codes in the operand buffer: thread
-// t takes token t % 64 and the quarter t / 64 of its code words.  Tokens at or
-// past the split end are whatever the ring holds there (finite codes; their
-// scores are masked and their V scales are zero).
-template <int D, typename G>
-__device__ __forceinline__ void um_codes_plane(uint32_t codes, uint8_t *dst)
+// One plane of a ring stage as the two fp16 operands whose sum is the plane's
+// values / 16, exactly: thread t takes token t % 64 and the quarter t / 64 of
+// its code words (all in one scale group).  q * (s_hi / 16) and q * (s_lo /
+// 16) are exact in fp16: s_hi keeps the top 7 significant bits of the fp16
+// scale s, s_lo = s - s_hi the rest (at most 4 bits), and |q| <= 8 takes at
+// most 4 (odd head_dim indices arrive as 16 q and take scale / 256).  Tokens
+// at or past n_valid get scale 0: zero operands.
+template <int D, int SB, typename G>
+__device__ __forceinline__ void um_split_plane(uint32_t codes, const uint8_t *scales, uint8_t *dst_hi, uint8_t *dst_lo,
+                                               int n_valid)
 {
     constexpr int WPT = D / 32;                      // code words per thread
     constexpr int NW = WPT < 4 ? WPT : 4;            // words per shared-memory load
     const int tok = threadIdx.x & (kUTile - 1), part = threadIdx.x >> 6;
+    const int g = (part * WPT) / 8;                  // the thread's scale group (64 values = 8 words)
+    __half sc = __ushort_as_half((unsigned short)0);
+    if (tok < n_valid) sc = reinterpret_cast<const __half *>(scales + tok * SB)[g];
+    const __half sh = __ushort_as_half((unsigned short)(__half_as_ushort(sc) & 0xFFF0u));
+    const __half sl = __hsub(sc, sh);
+    const __half2 k16 = __float2half2_rn(0.0625f), k256 = __float2half2_rn(0.00390625f);
+    const uint32_t h_e = h2_as_u32(__hmul2(__half2half2(sh), k16)), h_o = h2_as_u32(__hmul2(__half2half2(sh), k256));
+    const uint32_t l_e = h2_as_u32(__hmul2(__half2half2(sl), k16)), l_o = h2_as_u32(__hmul2(__half2half2(sl), k256));
 #pragma unroll
     for (int q = 0; q < WPT; q += NW) {
         const int w0 = part * WPT + q;               // first word, in 16-byte chunk w0 / 4 of the codes row
@@ -227,8 +237,21 @@ __device__ __forceinline__ void um_codes_plane(uint32_t codes, uint8_t *dst)
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(wv[0]), "=r"(wv[1]) : "r"(addr));
         }
 #pragma unroll
-        for (int i = 0; i < NW; ++i)
-            *reinterpret_cast<uint4 *>(dst + sw128_off(tok, w0 + i, kUTile * 128)) = codes_word(wv[i]);
+        for (int i = 0; i < NW; ++i) {
+            const uint4 c = codes_word(wv[i]);       // (q, q), (16q, 16q), (q, q), (16q, 16q)
+            uint4 hi, lo;
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi.x) : "r"(c.x), "r"(h_e));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi.y) : "r"(c.y), "r"(h_o));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi.z) : "r"(c.z), "r"(h_e));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi.w) : "r"(c.w), "r"(h_o));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.x) : "r"(c.x), "r"(l_e));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.y) : "r"(c.y), "r"(l_o));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.z) : "r"(c.z), "r"(l_e));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.w) : "r"(c.w), "r"(l_o));
+            const uint32_t off = sw128_off(tok, w0 + i, kUTile * 128);
+            *reinterpret_cast<uint4 *>(dst_hi + off) = hi;
+            *reinterpret_cast<uint4 *>(dst_lo + off) = lo;
+        }
     }
 }
 
@@ -239,15 +262,13 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     using C = UmCfg<D>;
     using KG = TileGeom<C::KRB>;
     using VG = TileGeom<C::VRB>;
-    constexpr int NS = C::NS, NG = C::NG;
+    constexpr int NS = C::NS;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + C::BAR_OFF, bar_s = bar_full + 8 * NS, bar_o = bar_s + 8;
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);     // [2][128]
-    float *ksf = reinterpret_cast<float *>(smem + C::SF_OFF);      // [NG][64] K scales x log2 units
-    float *vsf = ksf + NG * kUTile;                                // [NG][64] V scales (0 past the split end)
     __shared__ volatile int s_timeout;
     __shared__ int s_issued;
     __shared__ int s_seq;
@@ -318,8 +339,7 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         s_issued = first;
     }
     // the block's query rows as the A operand of S = Q K^T: fp16, head_dim in
-    // the unpack order inside each group of 8, odd indices divided by 16 (their
-    // K codes arrive as 16 q), 128-byte swizzled; rows >= R zero
+    // the unpack order inside each group of 8, 128-byte swizzled; rows >= R zero
     {
         const __half *q = static_cast<const __half *>(a.q);
         constexpr int CPR = D / 8;
@@ -328,7 +348,6 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             const int rr = r0 + row;
             qrow = (((int64_t)s * a.n_q + rr / G) * a.n_heads + kh * G + rr % G) * D;
         }
-        const __half2 k16 = __float2half2_rn(0.0625f);
 #pragma unroll 4
         for (int c = half * (CPR / 2); c < (half + 1) * (CPR / 2); ++c) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -338,8 +357,6 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.y) : "r"(v.x), "r"(v.z));   // (x1, x5)
             asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.z) : "r"(v.y), "r"(v.w));   // (x2, x6)
             asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.w) : "r"(v.y), "r"(v.w));   // (x3, x7)
-            o.y = h2_as_u32(__hmul2(u32_as_h2(o.y), k16));
-            o.w = h2_as_u32(__hmul2(u32_as_h2(o.w), k16));
             *reinterpret_cast<uint4 *>(smem + C::Q_OFF + sw128_off(row, c, C::Q_BLOCK)) = o;
         }
     }
@@ -347,75 +364,52 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     const int nv_row = row < R ? len + a.causal_extra - a.n_q + (r0 + row) / G + 1 : 0x7FFFFFFF;
     const int lim = min(hi, nv_row);
     float m_run = -INFINITY, l_part = 0.0f;
+    const float sc = a.scale_log2 * 16.0f;             // the K operands carry K / 16
 
     for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NS;
         const uint32_t stage = sbase + C::RING_OFF + st * C::STAGE;
         const uint8_t *stage_p = smem + C::RING_OFF + st * C::STAGE;
         uwait(bar_full + 8 * st, (j / NS) & 1, &s_timeout);
-        if (j > 0) uwait(bar_o, (j - 1) & 1, &s_timeout);     // O += P' V of the last tile read X and P'
+        if (j > 0) uwait(bar_o, (j - 1) & 1, &s_timeout);     // O += P V of the last tile read X and P
         tc_fence_after();
         const int tb = lo + j * kUTile;
         const int n_valid = min(kUTile, hi - tb);
-        // K codes into X; the tile's scales as fp32 (0 past the split end)
-        um_codes_plane<D, KG>(stage + C::SK_OFF, smem + C::X_OFF);
-        if (tid < NG * kUTile) {
-            const int g = tid / kUTile, t = tid % kUTile;
-            float kf = 0.0f, vf = 0.0f;
-            if (t < n_valid) {
-                kf = __half2float(reinterpret_cast<const __half *>(stage_p + C::SKS_OFF + t * C::KSB)[g]) * a.scale_log2;
-                vf = __half2float(reinterpret_cast<const __half *>(stage_p + C::SVS_OFF + t * C::VSB)[g]);
-            }
-            ksf[g * kUTile + t] = kf;
-            vsf[g * kUTile + t] = vf;
-        }
+        um_split_plane<D, C::KSB, KG>(stage + C::SK_OFF, stage_p + C::SKS_OFF, smem + C::X_OFF,
+                                      smem + C::X_OFF + C::X_PART, n_valid);
         async_proxy_fence();
         __syncthreads();
         if (tid == 0 && !s_timeout) {
-            // S_g = Q_g K_g^T, one accumulator per 64-value group
+            // S = Q K_hi^T + Q K_lo^T
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const int g = ks >> 2;
-                const uint64_t ad = umma_desc(sbase + C::Q_OFF + g * C::Q_BLOCK + (ks & 3) * 32, 16, 1024);
-                const uint64_t bd = umma_desc(sbase + C::X_OFF + g * C::X_BLOCK + (ks & 3) * 32, 16, 1024);
-                umma_f16(tmem + C::S_COL + 64 * g, ad, bd, C::IDESC_S, (ks & 3) ? 1u : 0u);
-            }
+            for (int hv = 0; hv < 2; ++hv)
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ad =
+                        umma_desc(sbase + C::Q_OFF + (ks >> 2) * C::Q_BLOCK + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = umma_desc(
+                        sbase + C::X_OFF + hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32, 16, 1024);
+                    umma_f16(tmem + C::S_COL, ad, bd, C::IDESC_S, (hv > 0 || ks > 0) ? 1u : 0u);
+                }
             umma_commit(bar_s);
         }
         uwait(bar_s, j & 1, &s_timeout);
         tc_fence_after();
-        // S = Q K^T has read X: the V codes go there now
-        um_codes_plane<D, VG>(stage + C::SV_OFF, smem + C::X_OFF);
-        // this thread's 32 scores: x = sum_g s_K(t, g) S_g, log2 units, masked
-        // past the split end and the row's causal limit
+        // S has read X: V_hi, V_lo go there now
+        um_split_plane<D, C::VSB, VG>(stage + C::SV_OFF, stage_p + C::SVS_OFF, smem + C::X_OFF,
+                                      smem + C::X_OFF + C::X_PART, n_valid);
+        // this thread's 32 scores (log2 units), masked past the split end and
+        // the row's causal limit
         float x[32];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            float sg[32];
-            tmem_ld32(lane_base + C::S_COL + 64 * g + 32 * half, sg);
-            const float4 *kf4 = reinterpret_cast<const float4 *>(ksf + g * kUTile + 32 * half);
-#pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 kf = kf4[i4];
-                if (g == 0) {
-                    x[4 * i4] = kf.x * sg[4 * i4];
-                    x[4 * i4 + 1] = kf.y * sg[4 * i4 + 1];
-                    x[4 * i4 + 2] = kf.z * sg[4 * i4 + 2];
-                    x[4 * i4 + 3] = kf.w * sg[4 * i4 + 3];
-                } else {
-                    x[4 * i4] = fmaf(kf.x, sg[4 * i4], x[4 * i4]);
-                    x[4 * i4 + 1] = fmaf(kf.y, sg[4 * i4 + 1], x[4 * i4 + 1]);
-                    x[4 * i4 + 2] = fmaf(kf.z, sg[4 * i4 + 2], x[4 * i4 + 2]);
-                    x[4 * i4 + 3] = fmaf(kf.w, sg[4 * i4 + 3], x[4 * i4 + 3]);
-                }
-            }
-        }
+        tmem_ld32(lane_base + C::S_COL + 32 * half, x);
         const int t0 = tb + 32 * half;
         if (t0 + 32 > lim) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (t0 + i >= lim) x[i] = -INFINITY;
+            for (int i = 0; i < 32; ++i) x[i] = (t0 + i < lim) ? x[i] * sc : -INFINITY;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= sc;
         }
         float mh = -INFINITY;
 #pragma unroll
@@ -432,29 +426,19 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         }
         l_part *= f;
         const float base = (m_run == -INFINITY) ? 0.0f : m_run;
+        uint32_t pk[16];
         float l_tile = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            x[i] = ex2(x[i] - base);
-            l_tile += x[i];
+        for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(x[2 * i] - base), p1 = ex2(x[2 * i + 1] - base);
+            l_tile += p0 + p1;
+            pk[i] = pack_f16x2(p0, p1);
         }
         l_part += l_tile;
-        // P'_g = p * s_V(t, g), rounded once to fp16, per V group
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            const float4 *vf4 = reinterpret_cast<const float4 *>(vsf + g * kUTile + 32 * half);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 vf = vf4[i4];
-                pk[2 * i4] = pack_f16x2(x[4 * i4] * vf.x, x[4 * i4 + 1] * vf.y);
-                pk[2 * i4 + 1] = pack_f16x2(x[4 * i4 + 2] * vf.z, x[4 * i4 + 3] * vf.w);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(smem + C::P_OFF + g * C::P_BLOCK + sw128_off(row, 4 * half + k, 0)) =
-                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4 *>(smem + C::P_OFF + sw128_off(row, 4 * half + k, 0)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         // O columns of this thread's half of head_dim, rescaled where the
         // maximum grew (whole warps: tensor-memory loads are warp-wide)
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -479,15 +463,16 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                          plane_row + lo + (int64_t)(j + NS) * kUTile);
                 s_issued = j + NS + 1;
             }
-            // O_g += P'_g V_g
+            // O += P V_hi + P V_lo
             tc_fence_after();
 #pragma unroll
-            for (int g = 0; g < NG; ++g)
+            for (int hv = 0; hv < 2; ++hv)
 #pragma unroll
                 for (int ks = 0; ks < kUTile / 16; ++ks) {
-                    const uint64_t ad = umma_desc(sbase + C::P_OFF + g * C::P_BLOCK + ks * 32, 16, 1024);
-                    const uint64_t bd = umma_desc(sbase + C::X_OFF + g * C::X_BLOCK + ks * 2048, C::X_BLOCK, 1024);
-                    umma_f16(tmem + C::O_COL + 64 * g, ad, bd, C::IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
+                    const uint64_t ad = umma_desc(sbase + C::P_OFF + ks * 32, 16, 1024);
+                    const uint64_t bd =
+                        umma_desc(sbase + C::X_OFF + hv * C::X_PART + ks * 2048, C::X_BLOCK, 1024);
+                    umma_f16(tmem + C::O_COL, ad, bd, C::IDESC_O, (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
                 }
             umma_commit(bar_o);
         }
@@ -500,8 +485,8 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     __syncthreads();
     const float L = red[row] + red[kURows + row];
     const bool empty = (m_run == -INFINITY || L <= 0.0f);
-    // the V codes entered as q (even head_dim index) and 16 q (odd)
-    const float inv = empty ? 0.0f : 1.0f / L, inv16 = inv * 0.0625f;
+    // the V operands carried V / 16
+    const float inv = empty ? 0.0f : 16.0f / L;
     const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
     float *dst = nullptr;
     int64_t orow = 0;
@@ -524,10 +509,10 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float *o = dst + half * (D / 2) + c + 8 * g;
-                *reinterpret_cast<float4 *>(o) = make_float4(ov[8 * g] * inv, ov[8 * g + 2] * inv16,
-                                                             ov[8 * g + 4] * inv, ov[8 * g + 6] * inv16);
-                *reinterpret_cast<float4 *>(o + 4) = make_float4(ov[8 * g + 1] * inv, ov[8 * g + 3] * inv16,
-                                                                 ov[8 * g + 5] * inv, ov[8 * g + 7] * inv16);
+                *reinterpret_cast<float4 *>(o) =
+                    make_float4(ov[8 * g] * inv, ov[8 * g + 2] * inv, ov[8 * g + 4] * inv, ov[8 * g + 6] * inv);
+                *reinterpret_cast<float4 *>(o + 4) =
+                    make_float4(ov[8 * g + 1] * inv, ov[8 * g + 3] * inv, ov[8 * g + 5] * inv, ov[8 * g + 7] * inv);
             }
         }
     }
