@@ -43,7 +43,8 @@ namespace kvq {
 using namespace ptx;
 namespace {
 
-constexpr int kUT = 256;                 // threads (8 warps)
+constexpr int kUT = 256;                 // compute threads (8 warps)
+constexpr int kUThreads = kUT + 32;      // + one warp that issues the MMAs and the tile copies
 constexpr int kURows = 128;              // query rows per CTA = tensor-memory lanes
 constexpr int kUTile = 64;               // tokens per tile (= the decode kernel's TMA box)
 
@@ -71,11 +72,29 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
                  : "memory");
 }
 
+// The same with the A operand in tensor memory (row i in lane i, two fp16 of
+// consecutive k per 32-bit column; one k-step of 16 is 8 columns).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// The compute warps' own barrier (the issuing warp never waits on it).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kUT) : "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -150,12 +169,11 @@ struct UmCfg {
     static constexpr int KSB = scale_row_bytes(KC, D), VSB = scale_row_bytes(VC, D);
     static constexpr int NG = D / 64;                             // 64-value blocks (= scale groups)
     // shared memory (from a 1024-aligned base)
-    static constexpr int Q_OFF = 0;                               // [NG][128 rows][128 B]
-    static constexpr int Q_BLOCK = kURows * 128;
-    static constexpr int X_OFF = Q_OFF + NG * Q_BLOCK;            // K, then V: [hi, lo][NG][64 tokens][128 B]
-    static constexpr int X_BLOCK = kUTile * 128;
+    static constexpr int X_BLOCK = kUTile * 128;                  // 64 tokens x 64 values, fp16
     static constexpr int X_PART = NG * X_BLOCK;
-    static constexpr int P_OFF = X_OFF + 2 * X_PART;              // P: [128 rows][64 tokens] fp16
+    static constexpr int XK_OFF = 0;                              // K operands: [hi, lo][NG][64 tokens][128 B]
+    static constexpr int XV_OFF = XK_OFF + 2 * X_PART;            // V operands, same layout
+    static constexpr int P_OFF = XV_OFF + 2 * X_PART;             // P: [128 rows][64 tokens] fp16
     static constexpr int RING_OFF = P_OFF + kURows * 128;
     // ring stage: K codes, V codes (TMA boxes), K scales, V scales
     static constexpr int SK_OFF = 0;
@@ -165,15 +183,20 @@ struct UmCfg {
     static constexpr int STAGE = align_up(SVS_OFF + kUTile * VSB, 1024);
     static constexpr int NS = 3;
     static constexpr int RED_OFF = RING_OFF + NS * STAGE;         // fp32 [2][128]: half-row maxima / sums
-    static constexpr int BAR_OFF = RED_OFF + 2 * kURows * 4;      // full[NS], S done, O done
-    static constexpr int TMEM_SLOT = BAR_OFF + (NS + 2) * 8;
+    // mbarriers: full[NS] (tile landed), S done, O done (MMA commits), K ready,
+    // P / V ready (the compute threads' hand-offs to the issuing warp)
+    static constexpr int BAR_OFF = RED_OFF + 2 * kURows * 4;
+    static constexpr int TMEM_SLOT = BAR_OFF + (NS + 4) * 8;
     static constexpr int SMEM = TMEM_SLOT + 16 + 1024;            // + alignment slack
-    // tensor memory: S in columns [0, 64), O in [64, 64 + D)
-    static constexpr int S_COL = 0, O_COL = 64;
-    static constexpr int NCOL = (64 + D) <= 128 ? 128 : (64 + D) <= 256 ? 256 : 512;
+    // tensor memory: O in [0, D), S double-buffered in [D, D + 128), the query
+    // rows (A operand of S = Q K^T, two fp16 per column) in [D + 128, D + 128 + D / 2)
+    static constexpr int O_COL = 0, S_COL = D, Q_COL = D + 128;
+    static constexpr int NCOL_USED = D + 128 + D / 2;
+    static constexpr int NCOL = NCOL_USED <= 128 ? 128 : NCOL_USED <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC_S = umma_idesc(kURows, kUTile, 0);
     static constexpr uint32_t IDESC_O = umma_idesc(kURows, D, 1);
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+    static_assert(NCOL_USED <= 512, "tensor memory");
 };
 
 // Bounded mbarrier wait that gives up for good once the CTA has timed out.
@@ -256,7 +279,7 @@ __device__ __forceinline__ void um_split_plane(uint32_t codes, const uint8_t *sc
 }
 
 template <int D>
-__global__ void __launch_bounds__(kUT, 1)
+__global__ void __launch_bounds__(kUThreads, 1)
 prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
 {
     using C = UmCfg<D>;
@@ -268,15 +291,17 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + C::BAR_OFF, bar_s = bar_full + 8 * NS, bar_o = bar_s + 8;
+    const uint32_t bar_k = bar_o + 8, bar_pv = bar_k + 8;
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);     // [2][128]
     __shared__ volatile int s_timeout;
     __shared__ int s_issued;
     __shared__ int s_seq;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool issuer = warp == kUT / 32;                           // the last warp
     // softmax and output: row (= tensor-memory lane) and which 32 tokens of a
     // tile / which half of head_dim this thread takes
-    const int row = tid & (kURows - 1), half = tid >> 7;
+    const int row = tid & (kURows - 1), half = (tid >> 7) & 1;
     const int split = blockIdx.x, kh = blockIdx.y / a.n_row_blocks, rblk = blockIdx.y % a.n_row_blocks;
     const int G = a.n_heads / a.n_kv_heads;
     const int r0 = rblk * kURows;
@@ -289,6 +314,8 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         for (int i = 0; i < NS; ++i) mbar_init(bar_full + 8 * i, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_k, kUT);
+        mbar_init(bar_pv, kUT);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -331,202 +358,245 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
     const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
     const uint8_t *vsc = reinterpret_cast<const uint8_t *>(a.v.sc);
-    if (tid == 0) {
-        const int first = min(NS, n_tiles);
-        for (int j = 0; j < first; ++j)
-            um_issue_tile<C, KG, VG>(sbase + C::RING_OFF + j * C::STAGE, bar_full + 8 * j, &tmk, &tmv, ksc, vsc,
-                                     plane_row + lo + (int64_t)j * kUTile);
-        s_issued = first;
-    }
-    // the block's query rows as the A operand of S = Q K^T: fp16, head_dim in
-    // the unpack order inside each group of 8, 128-byte swizzled; rows >= R zero
-    {
-        const __half *q = static_cast<const __half *>(a.q);
-        constexpr int CPR = D / 8;
-        int64_t qrow = 0;
-        if (row < R) {
-            const int rr = r0 + row;
-            qrow = (((int64_t)s * a.n_q + rr / G) * a.n_heads + kh * G + rr % G) * D;
-        }
-#pragma unroll 4
-        for (int c = half * (CPR / 2); c < (half + 1) * (CPR / 2); ++c) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < R) v = *reinterpret_cast<const uint4 *>(q + qrow + 8 * c);
-            uint4 o;
-            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.x) : "r"(v.x), "r"(v.z));   // (x0, x4)
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.y) : "r"(v.x), "r"(v.z));   // (x1, x5)
-            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.z) : "r"(v.y), "r"(v.w));   // (x2, x6)
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.w) : "r"(v.y), "r"(v.w));   // (x3, x7)
-            *reinterpret_cast<uint4 *>(smem + C::Q_OFF + sw128_off(row, c, C::Q_BLOCK)) = o;
-        }
-    }
-    // per-row softmax state (the two threads of a row keep the same maximum)
-    const int nv_row = row < R ? len + a.causal_extra - a.n_q + (r0 + row) / G + 1 : 0x7FFFFFFF;
-    const int lim = min(hi, nv_row);
-    float m_run = -INFINITY, l_part = 0.0f;
-    const float sc = a.scale_log2 * 16.0f;             // the K operands carry K / 16
+    auto stage_of = [&](int jj) { return C::RING_OFF + (jj % NS) * C::STAGE; };
 
-    for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NS;
-        const uint32_t stage = sbase + C::RING_OFF + st * C::STAGE;
-        const uint8_t *stage_p = smem + C::RING_OFF + st * C::STAGE;
-        uwait(bar_full + 8 * st, (j / NS) & 1, &s_timeout);
-        if (j > 0) uwait(bar_o, (j - 1) & 1, &s_timeout);     // O += P V of the last tile read X and P
-        tc_fence_after();
-        const int tb = lo + j * kUTile;
-        const int n_valid = min(kUTile, hi - tb);
-        um_split_plane<D, C::KSB, KG>(stage + C::SK_OFF, stage_p + C::SKS_OFF, smem + C::X_OFF,
-                                      smem + C::X_OFF + C::X_PART, n_valid);
-        async_proxy_fence();
-        __syncthreads();
-        if (tid == 0 && !s_timeout) {
-            // S = Q K_hi^T + Q K_lo^T
-            tc_fence_after();
-#pragma unroll
-            for (int hv = 0; hv < 2; ++hv)
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad =
-                        umma_desc(sbase + C::Q_OFF + (ks >> 2) * C::Q_BLOCK + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = umma_desc(
-                        sbase + C::X_OFF + hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32, 16, 1024);
-                    umma_f16(tmem + C::S_COL, ad, bd, C::IDESC_S, (hv > 0 || ks > 0) ? 1u : 0u);
-                }
-            umma_commit(bar_s);
-        }
-        uwait(bar_s, j & 1, &s_timeout);
-        tc_fence_after();
-        // S has read X: V_hi, V_lo go there now
-        um_split_plane<D, C::VSB, VG>(stage + C::SV_OFF, stage_p + C::SVS_OFF, smem + C::X_OFF,
-                                      smem + C::X_OFF + C::X_PART, n_valid);
-        // this thread's 32 scores (log2 units), masked past the split end and
-        // the row's causal limit
-        float x[32];
-        tmem_ld32(lane_base + C::S_COL + 32 * half, x);
-        const int t0 = tb + 32 * half;
-        if (t0 + 32 > lim) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = (t0 + i < lim) ? x[i] * sc : -INFINITY;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] *= sc;
-        }
-        float mh = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mh = fmaxf(mh, x[i]);
-        red[half * kURows + row] = mh;
-        __syncthreads();
-        const float mt = fmaxf(red[row], red[kURows + row]);
-        float f = 1.0f;
-        bool resc = false;
-        if (mt > m_run) {
-            f = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mt);
-            m_run = mt;
-            resc = true;
-        }
-        l_part *= f;
-        const float base = (m_run == -INFINITY) ? 0.0f : m_run;
-        uint32_t pk[16];
-        float l_tile = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(x[2 * i] - base), p1 = ex2(x[2 * i + 1] - base);
-            l_tile += p0 + p1;
-            pk[i] = pack_f16x2(p0, p1);
-        }
-        l_part += l_tile;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4 *>(smem + C::P_OFF + sw128_off(row, 4 * half + k, 0)) =
-                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        // O columns of this thread's half of head_dim, rescaled where the
-        // maximum grew (whole warps: tensor-memory loads are warp-wide)
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+    if (issuer) {
+        // ---- the issuing warp (one thread): tile copies and MMAs, in the order
+        // S(0); then per tile j: S(j + 1) as soon as its K operands are ready
+        // (it runs beside the softmax of tile j), O += P V of tile j as soon as
+        // P and the V operands are ready (and tile j's ring stage is refilled)
+        if ((tid & 31) == 0) {
+            const int first = min(NS, n_tiles);
+            for (int j = 0; j < first; ++j)
+                um_issue_tile<C, KG, VG>(sbase + stage_of(j), bar_full + 8 * j, &tmk, &tmv, ksc, vsc,
+                                         plane_row + lo + (int64_t)j * kUTile);
+            s_issued = first;
+            auto issue_s = [&](int jj) {
+                tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 2; c += 32) {
-                float ov[32];
-                const uint32_t ta = lane_base + C::O_COL + half * (D / 2) + c;
-                tmem_ld32(ta, ov);
+                for (int hv = 0; hv < 2; ++hv)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] *= f;
-                tmem_st32(ta, ov);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t bd = umma_desc(
+                            sbase + C::XK_OFF + hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32, 16, 1024);
+                        umma_f16_ta(tmem + C::S_COL + 64 * (jj & 1), tmem + C::Q_COL + 8 * ks, bd, C::IDESC_S,
+                                    (hv > 0 || ks > 0) ? 1u : 0u);
+                    }
+                umma_commit(bar_s);
+            };
+            if (n_tiles > 0 && uwait(bar_k, 0, &s_timeout)) issue_s(0);
+            for (int j = 0; j < n_tiles && !s_timeout; ++j) {
+                if (j + 1 < n_tiles) {
+                    if (!uwait(bar_k, (j + 1) & 1, &s_timeout)) break;
+                    issue_s(j + 1);
+                }
+                if (!uwait(bar_pv, j & 1, &s_timeout)) break;
+                if (j + NS < n_tiles) {
+                    um_issue_tile<C, KG, VG>(sbase + stage_of(j), bar_full + 8 * (j % NS), &tmk, &tmv, ksc, vsc,
+                                             plane_row + lo + (int64_t)(j + NS) * kUTile);
+                    s_issued = j + NS + 1;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int hv = 0; hv < 2; ++hv)
+#pragma unroll
+                    for (int ks = 0; ks < kUTile / 16; ++ks) {
+                        const uint64_t ad = umma_desc(sbase + C::P_OFF + ks * 32, 16, 1024);
+                        const uint64_t bd =
+                            umma_desc(sbase + C::XV_OFF + hv * C::X_PART + ks * 2048, C::X_BLOCK, 1024);
+                        umma_f16(tmem + C::O_COL, ad, bd, C::IDESC_O, (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
+                    }
+                umma_commit(bar_o);
+            }
+        }
+        __syncwarp();
+    }
+    else {
+        // ---- the compute warps
+        // the block's query rows into tensor memory as the A operand of S = Q K^T:
+        // fp16, head_dim in the unpack order inside each group of 8 (two values a
+        // column); rows >= R zero.  Thread (row, half) writes half of its row.
+        {
+            const __half *q = static_cast<const __half *>(a.q);
+            int64_t qrow = 0;
+            if (row < R) {
+                const int rr = r0 + row;
+                qrow = (((int64_t)s * a.n_q + rr / G) * a.n_heads + kh * G + rr % G) * D;
+            }
+#pragma unroll 1
+            for (int cb = 0; cb < D / 4; cb += 32) {              // 32 columns = 8 chunks of 8 values
+                float qc[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int c = half * (D / 16) + cb / 4 + k;   // value chunk
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (row < R) v = *reinterpret_cast<const uint4 *>(q + qrow + 8 * c);
+                    uint32_t o0, o1, o2, o3;
+                    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o0) : "r"(v.x), "r"(v.z));   // (x0, x4)
+                    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o1) : "r"(v.x), "r"(v.z));   // (x1, x5)
+                    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o2) : "r"(v.y), "r"(v.w));   // (x2, x6)
+                    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o3) : "r"(v.y), "r"(v.w));   // (x3, x7)
+                    qc[4 * k] = __uint_as_float(o0);
+                    qc[4 * k + 1] = __uint_as_float(o1);
+                    qc[4 * k + 2] = __uint_as_float(o2);
+                    qc[4 * k + 3] = __uint_as_float(o3);
+                }
+                tmem_st32(lane_base + C::Q_COL + half * (D / 4) + cb, qc);
             }
             tmem_st_wait();
         }
-        async_proxy_fence();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && !s_timeout) {
-            // the stage is free again (its V codes were read above): refill it
-            if (j + NS < n_tiles) {
-                um_issue_tile<C, KG, VG>(stage, bar_full + 8 * st, &tmk, &tmv, ksc, vsc,
-                                         plane_row + lo + (int64_t)(j + NS) * kUTile);
-                s_issued = j + NS + 1;
-            }
-            // O += P V_hi + P V_lo
-            tc_fence_after();
-#pragma unroll
-            for (int hv = 0; hv < 2; ++hv)
-#pragma unroll
-                for (int ks = 0; ks < kUTile / 16; ++ks) {
-                    const uint64_t ad = umma_desc(sbase + C::P_OFF + ks * 32, 16, 1024);
-                    const uint64_t bd =
-                        umma_desc(sbase + C::X_OFF + hv * C::X_PART + ks * 2048, C::X_BLOCK, 1024);
-                    umma_f16(tmem + C::O_COL, ad, bd, C::IDESC_O, (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
-                }
-            umma_commit(bar_o);
-        }
-    }
-    // the dependent launch (the merge of the splits) may start now
-    pdl_trigger();
-    if (n_tiles > 0) uwait(bar_o, (n_tiles - 1) & 1, &s_timeout);
-    tc_fence_after();
-    red[half * kURows + row] = l_part;
-    __syncthreads();
-    const float L = red[row] + red[kURows + row];
-    const bool empty = (m_run == -INFINITY || L <= 0.0f);
-    // the V operands carried V / 16
-    const float inv = empty ? 0.0f : 16.0f / L;
-    const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
-    float *dst = nullptr;
-    int64_t orow = 0;
-    if (row < R) {
-        const int rr = r0 + row;
-        orow = ((int64_t)s * a.n_q + rr / G) * a.n_heads + kh * G + rr % G;
-        dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
-    }
-#pragma unroll 1
-    for (int c = 0; c < D / 2; c += 32) {
-        float ov[32];
+        // per-row softmax state (the two threads of a row keep the same maximum)
+        const int nv_row = row < R ? len + a.causal_extra - a.n_q + (r0 + row) / G + 1 : 0x7FFFFFFF;
+        const int lim = min(hi, nv_row);
+        float m_run = -INFINITY, l_part = 0.0f;
+        const float sc = a.scale_log2 * 16.0f;         // the K operands carry K / 16
+        // hand-off to the issuing warp: this thread's shared-memory operand writes
+        // (and tensor-memory stores) are done
+        auto hand_off = [&](uint32_t bar) {
+            async_proxy_fence();
+            tc_fence_before();
+            mbar_arrive(bar);
+        };
+
+        // K operands of tile 0 (and, above, the query rows)
         if (n_tiles > 0) {
-            tmem_ld32(lane_base + C::O_COL + half * (D / 2) + c, ov);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = 0.0f;
+            uwait(bar_full, 0, &s_timeout);
+            um_split_plane<D, C::KSB, KG>(sbase + stage_of(0) + C::SK_OFF, smem + stage_of(0) + C::SKS_OFF,
+                                          smem + C::XK_OFF, smem + C::XK_OFF + C::X_PART, min(kUTile, hi - lo));
+            hand_off(bar_k);
         }
-        if (dst) {
-            // columns 8g + p hold head_dim 8g + (0, 4, 1, 5, 2, 6, 3, 7)[p]
+        for (int j = 0; j < n_tiles; ++j) {
+            const int tb = lo + j * kUTile;
+            // (1) the K operands of tile j + 1, once S of tile j has read the buffer
+            //     (runs beside O += P V of tile j - 1)
+            uwait(bar_s, j & 1, &s_timeout);
+            tc_fence_after();
+            if (j + 1 < n_tiles) {
+                uwait(bar_full + 8 * ((j + 1) % NS), ((j + 1) / NS) & 1, &s_timeout);
+                um_split_plane<D, C::KSB, KG>(sbase + stage_of(j + 1) + C::SK_OFF,
+                                              smem + stage_of(j + 1) + C::SKS_OFF, smem + C::XK_OFF,
+                                              smem + C::XK_OFF + C::X_PART, min(kUTile, hi - tb - kUTile));
+                hand_off(bar_k);
+            }
+            // (2) the V operands of tile j, once O += P V of tile j - 1 is done
+            if (j > 0) uwait(bar_o, (j - 1) & 1, &s_timeout);
+            tc_fence_after();
+            um_split_plane<D, C::VSB, VG>(sbase + stage_of(j) + C::SV_OFF, smem + stage_of(j) + C::SVS_OFF,
+                                          smem + C::XV_OFF, smem + C::XV_OFF + C::X_PART, min(kUTile, hi - tb));
+            // (3) softmax of tile j: this thread's 32 scores (log2 units), masked
+            //     past the split end and the row's causal limit
+            float x[32];
+            tmem_ld32(lane_base + C::S_COL + 64 * (j & 1) + 32 * half, x);
+            const int t0 = tb + 32 * half;
+            if (t0 + 32 > lim) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                float *o = dst + half * (D / 2) + c + 8 * g;
-                *reinterpret_cast<float4 *>(o) =
-                    make_float4(ov[8 * g] * inv, ov[8 * g + 2] * inv, ov[8 * g + 4] * inv, ov[8 * g + 6] * inv);
-                *reinterpret_cast<float4 *>(o + 4) =
-                    make_float4(ov[8 * g + 1] * inv, ov[8 * g + 3] * inv, ov[8 * g + 5] * inv, ov[8 * g + 7] * inv);
+                for (int i = 0; i < 32; ++i) x[i] = (t0 + i < lim) ? x[i] * sc : -INFINITY;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] *= sc;
+            }
+            float mh = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mh = fmaxf(mh, x[i]);
+            red[half * kURows + row] = mh;
+            compute_sync();
+            const float mt = fmaxf(red[row], red[kURows + row]);
+            float f = 1.0f;
+            bool resc = false;
+            if (mt > m_run) {
+                f = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mt);
+                m_run = mt;
+                resc = true;
+            }
+            l_part *= f;
+            const float base = (m_run == -INFINITY) ? 0.0f : m_run;
+            uint32_t pk[16];
+            float l_tile = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = ex2(x[2 * i] - base), p1 = ex2(x[2 * i + 1] - base);
+                l_tile += p0 + p1;
+                pk[i] = pack_f16x2(p0, p1);
+            }
+            l_part += l_tile;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(smem + C::P_OFF + sw128_off(row, 4 * half + k, 0)) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            // O columns of this thread's half of head_dim, rescaled where the
+            // maximum grew (whole warps: tensor-memory loads are warp-wide)
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 2; c += 32) {
+                    float ov[32];
+                    const uint32_t ta = lane_base + C::O_COL + half * (D / 2) + c;
+                    tmem_ld32(ta, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= f;
+                    tmem_st32(ta, ov);
+                }
+                tmem_st_wait();
+            }
+            // (4) P, the V operands and O are ready for O += P V of tile j; the
+            //     maxima buffer is reused by the next tile only after every
+            //     thread has read it (the next tile's first hand-off comes later
+            //     in program order than these reads, and the next write follows
+            //     a wait on O += P V, which needs every thread's hand-off)
+            hand_off(bar_pv);
+        }
+        // the dependent launch (the merge of the splits) may start now
+        pdl_trigger();
+        if (n_tiles > 0) uwait(bar_o, (n_tiles - 1) & 1, &s_timeout);
+        tc_fence_after();
+        compute_sync();
+        red[half * kURows + row] = l_part;
+        compute_sync();
+        const float L = red[row] + red[kURows + row];
+        const bool empty = (m_run == -INFINITY || L <= 0.0f);
+        // the V operands carried V / 16
+        const float inv = empty ? 0.0f : 16.0f / L;
+        const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
+        float *dst = nullptr;
+        int64_t orow = 0;
+        if (row < R) {
+            const int rr = r0 + row;
+            orow = ((int64_t)s * a.n_q + rr / G) * a.n_heads + kh * G + rr % G;
+            dst = (a.n_splits == 1) ? a.out + orow * D : a.part_o + ((int64_t)split * rows_total + orow) * D;
+        }
+#pragma unroll 1
+        for (int c = 0; c < D / 2; c += 32) {
+            float ov[32];
+            if (n_tiles > 0) {
+                tmem_ld32(lane_base + C::O_COL + half * (D / 2) + c, ov);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = 0.0f;
+            }
+            if (dst) {
+                // columns 8g + p hold head_dim 8g + (0, 4, 1, 5, 2, 6, 3, 7)[p]
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float *o = dst + half * (D / 2) + c + 8 * g;
+                    *reinterpret_cast<float4 *>(o) =
+                        make_float4(ov[8 * g] * inv, ov[8 * g + 2] * inv, ov[8 * g + 4] * inv, ov[8 * g + 6] * inv);
+                    *reinterpret_cast<float4 *>(o + 4) = make_float4(ov[8 * g + 1] * inv, ov[8 * g + 3] * inv,
+                                                                     ov[8 * g + 5] * inv, ov[8 * g + 7] * inv);
+                }
             }
         }
-    }
-    if (dst && half == 0) {
-        const float lse = empty ? -INFINITY : (m_run + log2f(L)) * kLn2;
-        if (a.n_splits == 1) {
-            if (a.out_lse) a.out_lse[orow] = lse;
-        } else {
-            a.part_lse[(int64_t)split * rows_total + orow] = lse;
+        if (dst && half == 0) {
+            const float lse = empty ? -INFINITY : (m_run + log2f(L)) * kLn2;
+            if (a.n_splits == 1) {
+                if (a.out_lse) a.out_lse[orow] = lse;
+            } else {
+                a.part_lse[(int64_t)split * rows_total + orow] = lse;
+            }
         }
     }
     // never leave while a copy into shared memory could be in flight (only
     // possible after a timeout)
-    if (tid == 0 && s_timeout) {
+    __syncthreads();
+    if (tid == kUT && s_timeout) {
         const int issued = s_issued;
         for (int j = issued - 1; j >= 0 && j >= issued - NS; --j) mbar_wait(bar_full + 8 * (j % NS), (j / NS) & 1);
         if (a.err) atomicOr(a.err, KVQ_ERR_TIMEOUT);
@@ -552,7 +622,7 @@ int um_ctas_per_sm()
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (r != cudaSuccess) return -(int)r;
         int v = 0;
-        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kUT, C::SMEM);
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kUThreads, C::SMEM);
         if (r != cudaSuccess) return -(int)r;
         // the CTAs sharing an SM must fit its 512 tensor-memory columns
         if (v * C::NCOL > 512) v = 512 / C::NCOL;
@@ -575,7 +645,7 @@ cudaError_t um_launch(const DecodeArgs &a, cudaStream_t st)
     if (!make_codes_map(&tk, a.k.qs, C::KRB, rows, kUTile) || !make_codes_map(&tv, a.v.qs, C::VRB, rows, kUTile))
         return cudaErrorInvalidValue;
     dim3 grid(a.n_splits, a.n_kv_heads * a.n_row_blocks, a.n_seq);
-    return launch_pdl(prefill_umma_kernel<D>, grid, dim3(kUT), C::SMEM, st, a, tk, tv);
+    return launch_pdl(prefill_umma_kernel<D>, grid, dim3(kUThreads), C::SMEM, st, a, tk, tv);
 }
 
 }  // namespace
