@@ -97,6 +97,21 @@ int resolve_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int3
     int per_sm = umma ? kvq::prefill_umma_ctas_per_sm(k->codec, v->codec, k->head_dim)
                       : kvq::decode_ctas_per_sm(k->codec, v->codec, k->head_dim, rows);
     if (per_sm <= 0) per_sm = 3;
+    if (umma) {
+        // one CTA per SM and many tiles per CTA: the split count whose waves
+        // divide the work most evenly (ceil(units * s / slots) / s smallest, the
+        // fewest splits among equals; at most 8, so the partials stay small).
+        // 96 units on 152 SMs: 3 splits, 2 full waves.
+        const int64_t slots = (int64_t)per_sm * sm_count();
+        const int64_t max_s = kvq::ceil_div(max_kv_len, 256) < 8 ? kvq::ceil_div(max_kv_len, 256) : 8;
+        int64_t best = 1;
+        double best_cost = 1e30;
+        for (int64_t c = 1; c <= (max_s > 1 ? max_s : 1); ++c) {
+            const double cost = (double)kvq::ceil_div(units * c, slots) / (double)c;
+            if (cost < best_cost - 1e-9) best_cost = cost, best = c;
+        }
+        return (int)best;
+    }
     int64_t target;
     if (k->n_seq == 1) {
         // one wave of the decode kernel's CTAs
