@@ -371,17 +371,21 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                 um_issue_tile<C, KG, VG>(sbase + stage_of(j), bar_full + 8 * j, &tmk, &tmv, ksc, vsc,
                                          plane_row + lo + (int64_t)j * kUTile);
             s_issued = first;
+            // descriptors: built once; a k-step adds a constant to the start
+            // address field (16-byte units, no carry: shared memory < 256 KB)
+            const uint64_t kdesc = umma_desc(sbase + C::XK_OFF, 16, 1024);
+            const uint64_t vdesc = umma_desc(sbase + C::XV_OFF, C::X_BLOCK, 1024);
+            const uint64_t pdesc = umma_desc(sbase + C::P_OFF, 16, 1024);
             auto issue_s = [&](int jj) {
                 tc_fence_after();
-#pragma unroll 1
+                const uint32_t d = tmem + C::S_COL + 64 * (jj & 1);
+#pragma unroll
                 for (int hv = 0; hv < 2; ++hv)
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t bd = umma_desc(
-                            sbase + C::XK_OFF + hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32, 16, 1024);
-                        umma_f16_ta(tmem + C::S_COL + 64 * (jj & 1), tmem + C::Q_COL + 8 * ks, bd, C::IDESC_S,
-                                    (hv > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_f16_ta(d, tmem + C::Q_COL + 8 * ks,
+                                    kdesc + (uint64_t)((hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32) >> 4),
+                                    C::IDESC_S, (hv > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_s);
             };
             if (n_tiles > 0 && uwait(bar_k, 0, &s_timeout)) issue_s(0);
@@ -397,15 +401,13 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                     s_issued = j + NS + 1;
                 }
                 tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int hv = 0; hv < 2; ++hv)
 #pragma unroll
-                    for (int ks = 0; ks < kUTile / 16; ++ks) {
-                        const uint64_t ad = umma_desc(sbase + C::P_OFF + ks * 32, 16, 1024);
-                        const uint64_t bd =
-                            umma_desc(sbase + C::XV_OFF + hv * C::X_PART + ks * 2048, C::X_BLOCK, 1024);
-                        umma_f16(tmem + C::O_COL, ad, bd, C::IDESC_O, (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < kUTile / 16; ++ks)
+                        umma_f16(tmem + C::O_COL, pdesc + (uint64_t)((ks * 32) >> 4),
+                                 vdesc + (uint64_t)((hv * C::X_PART + ks * 2048) >> 4), C::IDESC_O,
+                                 (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_o);
             }
         }
