@@ -62,6 +62,16 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _bf16_peak():
+    """The measured dense bf16 burst rate (TFLOP/s): the peak of an fp16 tensor
+    contraction timed alone (fp16 and bf16 run at the same nominal rate)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError, TypeError):
+        return 1900.0, "fallback"
+
+
 # The sources of the kernels the committed captures profile (the Q4_G64 decode
 # and the merge) and of their launch (split policy, tensor maps).
 _PROFILED_SOURCES = ("kvq_api.cu", "kvq_decode_common.cuh", "kvq_decode_tc.cu", "kvq_decode_tc.cuh",
@@ -603,6 +613,8 @@ def run_ours(args, wl, kv_bytes, world, rank, local):
             torch.cuda.empty_cache()
         also["long196k_host_tier"] = host_tier_summary(args, dev, peak)
         torch.cuda.empty_cache()
+        also["prefill512_32k"] = prefill_summary(args, dev)
+        torch.cuda.empty_cache()
         res["also"] = also
     return res
 
@@ -666,6 +678,66 @@ def host_tier_summary(args, dev, peak, resident_frac=0.5, page_tokens=8192, n_sl
             "timing": f"events around {reps} eager calls on the caller's stream"}
 
 
+def prefill_summary(args, dev, n_new=512, total=32768):
+    """A prompt chunk through kvq_decode_attention: n_new new tokens of 24 query
+    heads over 4 kv heads (head_dim 256, Q4_G64 K/V, fp16 queries) attending
+    causally to the total - n_new cached keys and to each other (the
+    tensor-core prompt-chunk kernel, default splits).  Graph of back-to-back
+    calls, events around replays; FLOPs = 4 * head_dim * (visible keys summed
+    over query rows)."""
+    import torch
+    import quantized_kv_cache_q4_gb300 as kvq
+    H, Hk, D = 24, 4, 256
+    sp = workloads.Spec("prefill512_32k", 1, H, Hk, D, (total - n_new,), n_new, workloads.Q4_G64,
+                        workloads.Q4_G64, "f16", "f16", "normal", workloads.BASE_SEED + 900)
+    wl = workloads.make(sp)
+    k = kvq.KVCache(sp.k_codec, 1, Hk, D, wl.capacity, device=dev)
+    v = kvq.KVCache(sp.v_codec, 1, Hk, D, wl.capacity, device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    src = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)   # noqa: E731
+    kvq.kvq_quantize_append(k, v, src(wl.k_prefill[0][None]), src(wl.v_prefill[0][None]), int(wl.cached_len[0]), zero)
+    kvq.kvq_quantize_append(k, v, src(wl.k_new), src(wl.v_new), n_new, src(wl.cached_len))
+    torch.cuda.synchronize()
+    q, kv_len = src(wl.q), src(wl.kv_len)
+    out = torch.empty((1, n_new, H, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, n_new, H), dtype=torch.float32, device=dev)
+    n_splits = kvq.kvq_decode_default_splits(k, v, H, n_new, total)
+    ws = kvq.alloc_workspace(kvq.kvq_decode_workspace_bytes(k, v, H, n_new, total, 0), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        kvq.kvq_decode_attention(k, v, q, n_new, H, sp.scale, kv_len, total, 0, out, lse, ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    reps = 10
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            call()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(5):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / reps)
+    visible = sum(total - n_new + i + 1 for i in range(n_new)) * H
+    tflops = 4.0 * D * visible / (best * 1e-3) / 1e12
+    peak, kind = _bf16_peak()
+    return {"workload": f"prompt chunk of {n_new} tokens x 24 query heads over {total} keys (4 kv heads, head_dim "
+                        f"256, Q4_G64 K/V, fp16 queries)", "n_splits": n_splits,
+            "attention_us": round(best * 1e3, 3),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4), "peak_kind": f"{kind} bf16 dense burst (fp16 runs at the "
+                                                                      "same nominal rate)"},
+            "timing": f"graph of {reps} back-to-back calls, best of 5 replays"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -678,6 +750,8 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed replays before the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="measure the selected workload only")
+    ap.add_argument("--prefill", type=int, default=None, metavar="KEYS",
+                    help="measure only a 512-token prompt chunk over KEYS keys and print its summary")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = _dist_env()
@@ -692,6 +766,10 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
+    if args.prefill is not None:
+        if rank == 0:
+            print(json.dumps(prefill_summary(args, f"cuda:{local}", total=args.prefill)), flush=True)
+        return
     if world > 1:
         import torch
         import torch.distributed as dist
