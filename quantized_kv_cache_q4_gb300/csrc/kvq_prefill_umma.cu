@@ -170,10 +170,10 @@ struct UmCfg {
     static constexpr int NG = D / 64;                             // 64-value blocks (= scale groups)
     // shared memory (from a 1024-aligned base)
     static constexpr int X_BLOCK = kUTile * 128;                  // 64 tokens x 64 values, fp16
-    static constexpr int X_PART = NG * X_BLOCK;
-    static constexpr int XK_OFF = 0;                              // K operands: [hi, lo][NG][64 tokens][128 B]
-    static constexpr int XV_OFF = XK_OFF + 2 * X_PART;            // V operands, same layout
-    static constexpr int P_OFF = XV_OFF + 2 * X_PART;             // P: [128 rows][64 tokens] fp16
+    static constexpr int X_PAIR = 2 * X_BLOCK;                    // the hi and lo blocks of 64 values
+    static constexpr int XK_OFF = 0;                              // K operands: [NG][hi, lo][64 tokens][128 B]
+    static constexpr int XV_OFF = XK_OFF + NG * X_PAIR;           // V operands, same layout
+    static constexpr int P_OFF = XV_OFF + NG * X_PAIR;            // P: [128 rows][64 tokens] fp16
     static constexpr int RING_OFF = P_OFF + kURows * 128;
     // ring stage: K codes, V codes (TMA boxes), K scales, V scales
     static constexpr int SK_OFF = 0;
@@ -188,12 +188,13 @@ struct UmCfg {
     static constexpr int BAR_OFF = RED_OFF + 2 * kURows * 4;
     static constexpr int TMEM_SLOT = BAR_OFF + (NS + 4) * 8;
     static constexpr int SMEM = TMEM_SLOT + 16 + 1024;            // + alignment slack
-    // tensor memory: O in [0, D), S double-buffered in [D, D + 128), the query
-    // rows (A operand of S = Q K^T, two fp16 per column) in [D + 128, D + 128 + D / 2)
+    // tensor memory: O in [0, D); the scores against K_hi (64 columns) and
+    // against K_lo (the next 64) in [D, D + 128); the query rows (A operand of
+    // S, two fp16 per column) in [D + 128, D + 128 + D / 2)
     static constexpr int O_COL = 0, S_COL = D, Q_COL = D + 128;
     static constexpr int NCOL_USED = D + 128 + D / 2;
     static constexpr int NCOL = NCOL_USED <= 128 ? 128 : NCOL_USED <= 256 ? 256 : 512;
-    static constexpr uint32_t IDESC_S = umma_idesc(kURows, kUTile, 0);
+    static constexpr uint32_t IDESC_S = umma_idesc(kURows, 2 * kUTile, 0);
     static constexpr uint32_t IDESC_O = umma_idesc(kURows, D, 1);
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
     static_assert(NCOL_USED <= 512, "tensor memory");
@@ -226,15 +227,15 @@ __device__ __forceinline__ void um_issue_tile(uint32_t st, uint32_t full, const 
 }
 
 // One plane of a ring stage as the two fp16 operands whose sum is the plane's
-// values / 16, exactly: thread t takes token t % 64 and the quarter t / 64 of
-// its code words (all in one scale group).  q * (s_hi / 16) and q * (s_lo /
+// values / 16, exactly, stored per block of 64 values as the hi rows of the 64
+// tokens followed by their lo rows: thread t takes token t % 64 and the
+// quarter t / 64 of its code words (all in one scale group).  q * (s_hi / 16) and q * (s_lo /
 // 16) are exact in fp16: s_hi keeps the top 7 significant bits of the fp16
 // scale s, s_lo = s - s_hi the rest (at most 4 bits), and |q| <= 8 takes at
 // most 4 (odd head_dim indices arrive as 16 q and take scale / 256).  Tokens
 // at or past n_valid get scale 0: zero operands.
 template <int D, int SB, typename G>
-__device__ __forceinline__ void um_split_plane(uint32_t codes, const uint8_t *scales, uint8_t *dst_hi, uint8_t *dst_lo,
-                                               int n_valid)
+__device__ __forceinline__ void um_split_plane(uint32_t codes, const uint8_t *scales, uint8_t *dst, int n_valid)
 {
     constexpr int WPT = D / 32;                      // code words per thread
     constexpr int NW = WPT < 4 ? WPT : 4;            // words per shared-memory load
@@ -271,9 +272,10 @@ __device__ __forceinline__ void um_split_plane(uint32_t codes, const uint8_t *sc
             asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.y) : "r"(c.y), "r"(l_o));
             asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.z) : "r"(c.z), "r"(l_e));
             asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(lo.w) : "r"(c.w), "r"(l_o));
-            const uint32_t off = sw128_off(tok, w0 + i, kUTile * 128);
-            *reinterpret_cast<uint4 *>(dst_hi + off) = hi;
-            *reinterpret_cast<uint4 *>(dst_lo + off) = lo;
+            // [block of 64 values][hi, lo][token][128 B]
+            const uint32_t off = sw128_off(tok, w0 + i, 2 * kUTile * 128);
+            *reinterpret_cast<uint4 *>(dst + off) = hi;
+            *reinterpret_cast<uint4 *>(dst + off + kUTile * 128) = lo;
         }
     }
 }
@@ -374,18 +376,18 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             // descriptors: built once; a k-step adds a constant to the start
             // address field (16-byte units, no carry: shared memory < 256 KB)
             const uint64_t kdesc = umma_desc(sbase + C::XK_OFF, 16, 1024);
-            const uint64_t vdesc = umma_desc(sbase + C::XV_OFF, C::X_BLOCK, 1024);
+            const uint64_t vdesc = umma_desc(sbase + C::XV_OFF, C::X_PAIR, 1024);
             const uint64_t pdesc = umma_desc(sbase + C::P_OFF, 16, 1024);
+            // S = Q [K_hi; K_lo]^T: N = 128 (the hi rows of the tile's 64 tokens,
+            // then their lo rows), one accumulator; the compute warps add the halves
             auto issue_s = [&](int jj) {
+                (void)jj;
                 tc_fence_after();
-                const uint32_t d = tmem + C::S_COL + 64 * (jj & 1);
 #pragma unroll
-                for (int hv = 0; hv < 2; ++hv)
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        umma_f16_ta(d, tmem + C::Q_COL + 8 * ks,
-                                    kdesc + (uint64_t)((hv * C::X_PART + (ks >> 2) * C::X_BLOCK + (ks & 3) * 32) >> 4),
-                                    C::IDESC_S, (hv > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_f16_ta(tmem + C::S_COL, tmem + C::Q_COL + 8 * ks,
+                                kdesc + (uint64_t)(((ks >> 2) * C::X_PAIR + (ks & 3) * 32) >> 4), C::IDESC_S,
+                                ks > 0 ? 1u : 0u);
                 umma_commit(bar_s);
             };
             if (n_tiles > 0 && uwait(bar_k, 0, &s_timeout)) issue_s(0);
@@ -406,7 +408,7 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
                     for (int ks = 0; ks < kUTile / 16; ++ks)
                         umma_f16(tmem + C::O_COL, pdesc + (uint64_t)((ks * 32) >> 4),
-                                 vdesc + (uint64_t)((hv * C::X_PART + ks * 2048) >> 4), C::IDESC_O,
+                                 vdesc + (uint64_t)((hv * C::X_BLOCK + ks * 2048) >> 4), C::IDESC_O,
                                  (j > 0 || hv > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_o);
             }
@@ -464,31 +466,38 @@ prefill_umma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         if (n_tiles > 0) {
             uwait(bar_full, 0, &s_timeout);
             um_split_plane<D, C::KSB, KG>(sbase + stage_of(0) + C::SK_OFF, smem + stage_of(0) + C::SKS_OFF,
-                                          smem + C::XK_OFF, smem + C::XK_OFF + C::X_PART, min(kUTile, hi - lo));
+                                          smem + C::XK_OFF, min(kUTile, hi - lo));
             hand_off(bar_k);
         }
         for (int j = 0; j < n_tiles; ++j) {
             const int tb = lo + j * kUTile;
-            // (1) the K operands of tile j + 1, once S of tile j has read the buffer
-            //     (runs beside O += P V of tile j - 1)
+            // (1) this thread's 32 scores of tile j (the K_hi and K_lo halves
+            //     added), then the K operands of tile j + 1 (S of tile j has read
+            //     the buffer; the hand-off also frees S for tile j + 1)
             uwait(bar_s, j & 1, &s_timeout);
             tc_fence_after();
+            float x[32];
+            {
+                float xl[32];
+                tmem_ld32(lane_base + C::S_COL + 32 * half, x);
+                tmem_ld32(lane_base + C::S_COL + 64 + 32 * half, xl);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] += xl[i];
+            }
             if (j + 1 < n_tiles) {
                 uwait(bar_full + 8 * ((j + 1) % NS), ((j + 1) / NS) & 1, &s_timeout);
                 um_split_plane<D, C::KSB, KG>(sbase + stage_of(j + 1) + C::SK_OFF,
                                               smem + stage_of(j + 1) + C::SKS_OFF, smem + C::XK_OFF,
-                                              smem + C::XK_OFF + C::X_PART, min(kUTile, hi - tb - kUTile));
+                                              min(kUTile, hi - tb - kUTile));
                 hand_off(bar_k);
             }
             // (2) the V operands of tile j, once O += P V of tile j - 1 is done
             if (j > 0) uwait(bar_o, (j - 1) & 1, &s_timeout);
             tc_fence_after();
             um_split_plane<D, C::VSB, VG>(sbase + stage_of(j) + C::SV_OFF, smem + stage_of(j) + C::SVS_OFF,
-                                          smem + C::XV_OFF, smem + C::XV_OFF + C::X_PART, min(kUTile, hi - tb));
-            // (3) softmax of tile j: this thread's 32 scores (log2 units), masked
-            //     past the split end and the row's causal limit
-            float x[32];
-            tmem_ld32(lane_base + C::S_COL + 64 * (j & 1) + 32 * half, x);
+                                          smem + C::XV_OFF, min(kUTile, hi - tb));
+            // (3) softmax of tile j: scores in log2 units, masked past the split
+            //     end and the row's causal limit
             const int t0 = tb + 32 * half;
             if (t0 + 32 > lim) {
 #pragma unroll
