@@ -111,10 +111,8 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
                          float *out, float *out_lse, cudaStream_t st)
 {
     if (rows == 0) return cudaSuccess;
-    // lanes per column: enough that a lane loads at most two rounds of kUnroll
-    // splits, fewer while that would take more than about a quarter wave of
-    // threads (measured on GB300: 114 splits x 24 rows is fastest with 16 lanes,
-    // 29 splits x 1152 rows with one lane per column)
+    // lanes per column: enough that a lane loads one round of kUnroll splits,
+    // fewer while that would take more than about a quarter wave of threads
     static PerDevice pd;
     int dev = 0;
     int n_sm = 0;
@@ -125,7 +123,7 @@ cudaError_t launch_merge(const float *po, const float *pl, int n_splits, int row
         });
     if (n_sm <= 0) n_sm = 152;
     int lpc = 1;
-    while (lpc < 32 && lpc * 2 * kUnroll < n_splits) lpc *= 2;
+    while (lpc < 32 && lpc * kUnroll < n_splits) lpc *= 2;
     const int64_t items = (int64_t)rows * (head_dim / 4);
     while (lpc > 1 && items * lpc > (int64_t)n_sm * 512) lpc /= 2;
     switch (lpc) {
