@@ -72,10 +72,10 @@ def _bf16_peak():
         return 1900.0, "fallback"
 
 
-# The sources of the kernels the committed captures profile (the Q4_G64 decode
-# and the merge) and of their launch (split policy, tensor maps).
+# The sources of the kernels the committed captures profile (the decode
+# kernels and the merge) and of their launch (split policy, tensor maps).
 _PROFILED_SOURCES = ("kvq_api.cu", "kvq_decode_common.cuh", "kvq_decode_tc.cu", "kvq_decode_tc.cuh",
-                     "kvq_internal.cuh", "kvq_merge.cu", "kvq_ptx.cuh", "kvq_tensor_map.cu")
+                     "kvq_decode_warp.cu", "kvq_internal.cuh", "kvq_merge.cu", "kvq_ptx.cuh", "kvq_tensor_map.cu")
 
 
 def _kernel_hash() -> str:

@@ -502,13 +502,14 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     for (int idx = threadIdx.x; idx < R * (D / 4); idx += C::NTH) {
         const int r = idx / (D / 4), d = 4 * (idx % (D / 4)), g = d / 64;
         // common maximum of row r and each warp's weight
+        // (rolled loops: this code runs once per CTA, from a cold instruction cache)
         float M = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int w = 0; w < kWW; ++w) M = fmaxf(M, red[w * 16 + r]);
         float L = 0.0f, P = 0.0f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
-#pragma unroll
+#pragma unroll 2
             for (int w = 0; w < kWW; ++w) {
                 const float mw = red[w * 16 + r];
                 const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
