@@ -40,38 +40,47 @@ using namespace ptx;
 namespace {
 
 constexpr int kBlk = 16;            // tokens per warp block (one MMA row tile)
-constexpr int kSBlk = 2;            // blocks per ring stage (one copy of 32 rows)
 constexpr int kWW = 12;             // warps per CTA
 constexpr int kWMinBlocks = 1;      // CTAs per SM
 constexpr int kWS = 2;              // ring stages per warp
 constexpr int kWRows = 8;           // query rows per kv head (one n-tile)
 
-template <int D, typename QT>
+template <int KC, int D, typename QT>
 struct WCfg {
-    static constexpr int NG = D / 64;                 // Q4_G64 groups per row
-    static constexpr int RB = D / 2;                  // code bytes per row
-    static constexpr int CBB = kBlk * RB;             // code bytes of a block (K or V)
-    static constexpr int SBB = kBlk * NG * 2;         // scale bytes of a block (K or V)
-    static constexpr int CB = kSBlk * CBB;            // ... of a stage
-    static constexpr int SB = kSBlk * SBB;
+    static constexpr int NGK = D / group_size(KC);    // K scale groups per row
+    static constexpr int NGV = D / 64;                // V (Q4_G64) scale groups per row
+    static constexpr int KRB = row_bytes(KC, D);      // code bytes per row
+    static constexpr int VRB = D / 2;
+    static constexpr int KBI = KRB < 128 ? KRB : 128; // K box width (bytes); K rows of 256 bytes take two boxes
+    static constexpr int KNB = KRB / KBI;
+    static constexpr int KSTEPS_G = group_size(KC) / 16;                // MMA k-steps per K group
+    // blocks per ring stage: two (one copy of 32 rows) for 4-bit K, one for
+    // q8_0 K, whose stages are twice as large
+    static constexpr int SBLK = KC == KVQ_CODEC_Q8_0 ? 1 : 2;
+    static constexpr int ST = SBLK * kBlk;           // rows per stage
+    static constexpr int CBK = ST * KRB, CBV = ST * VRB;               // code bytes of a stage
+    static constexpr int SBKB = kBlk * NGK * 2, SBVB = kBlk * NGV * 2;  // scale bytes of a block
+    static constexpr int SBK = SBLK * SBKB, SBV = SBLK * SBVB;
     static constexpr int NSLOT = kWW * kWS;
     static constexpr int NTH = kWW * 32;
     static constexpr bool QLO = sizeof(QT) == 4;      // fp32 query: hi + lo fp16 parts
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + NSLOT * CB;
-    static constexpr int KS_OFF = V_OFF + NSLOT * CB;
-    static constexpr int VS_OFF = KS_OFF + NSLOT * SB;
-    static constexpr int QP_OFF = align_up(VS_OFF + NSLOT * SB, 128);    // fp16 [8][D] permuted, swizzled
-    static constexpr int QPL_OFF = QP_OFF + kWRows * D * 2;              // its low part (fp32 query)
-    static constexpr int KB_OFF = QPL_OFF + (QLO ? kWRows * D * 2 : 0);  // fp32 [NG][8] minus the K bias terms
-    static constexpr int QST_OFF = KB_OFF + align_up(NG * kWRows * 4, 16);   // the query rows as given
+    static constexpr int V_OFF = K_OFF + NSLOT * CBK;
+    static constexpr int KS_OFF = V_OFF + NSLOT * CBV;
+    static constexpr int VS_OFF = KS_OFF + NSLOT * SBK;
+    static constexpr int QP_OFF = align_up(VS_OFF + NSLOT * SBV, 128);  // fp16 [8][D] permuted, swizzled
+    static constexpr int QPL_OFF = QP_OFF + kWRows * D * 2;            // its low part (fp32 query)
+    static constexpr int KB_OFF = QPL_OFF + (QLO ? kWRows * D * 2 : 0);  // fp32 [NGK][8] minus the K bias terms
+    // the same as accumulator inputs, [NGK][tig][4] = (row 2 tig, 2 tig + 1, 2 tig, 2 tig + 1)
+    static constexpr int KBD_OFF = KB_OFF + align_up(NGK * kWRows * 4, 16);
+    static constexpr int QST_OFF = KBD_OFF + NGK * 64;                  // the query rows as given
     static constexpr int RED_OFF = QST_OFF + kWRows * D * (int)sizeof(QT);   // fp32 [kWW][16]: m, l per row
-    static constexpr int PSR_OFF = RED_OFF + kWW * 16 * 4;                   // fp32 [kWW][NG][8]: sums of P'
-    static constexpr int BAR_OFF = align_up(PSR_OFF + kWW * NG * 8 * 4, 16);
+    static constexpr int PSR_OFF = RED_OFF + kWW * 16 * 4;                   // fp32 [kWW][NGV][8]: sums of P'
+    static constexpr int BAR_OFF = align_up(PSR_OFF + kWW * NGV * 8 * 4, 16);
     static constexpr int SMEM = BAR_OFF + (NSLOT + 1) * 8 + 1024;           // + alignment slack
     // each warp's O for the combine, fp32 [8][D], over its own K ring (which
     // no other warp touches, so it may write while the others still stream)
-    static_assert(kWRows * D * 4 == kWS * CB, "a warp's O fills its K ring");
+    static_assert(kWRows * D * 4 == kWS * CBK, "a warp's O fills its K ring");
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -89,11 +98,24 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
-// NG fp16 scales (NG = 1, 2 or 4) at a shared address as raw words
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// NG fp16 scales (NG = 1, 2, 4 or 8) at a shared address as raw words
 template <int NG>
 __device__ __forceinline__ void lds_scales(uint32_t addr, uint32_t (&w)[(NG + 1) / 2])
 {
-    if constexpr (NG == 4) {
+    if constexpr (NG == 8) {
+        const uint4 v = lds128(addr);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else if constexpr (NG == 4) {
         const uint2 v = lds64(addr);
         w[0] = v.x;
         w[1] = v.y;
@@ -118,21 +140,26 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
     return y;
 }
 
-template <int D, typename QT>
+template <int KC, int D, typename QT>
 __global__ void __launch_bounds__(kWW * 32, kWMinBlocks)
 decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
 {
-    using C = WCfg<D, QT>;
-    constexpr int NG = C::NG;
-    using TG = TileGeom<C::RB>;
+    using C = WCfg<KC, D, QT>;
+    constexpr int NGK = C::NGK, NGV = C::NGV;
+    constexpr bool K8 = (KC == KVQ_CODEC_Q8_0);
+    using KG = TileGeom<C::KBI>;
+    using VG = TileGeom<C::VRB>;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the base rounded up to 1024 bytes by pointer arithmetic on the shared
+    // array, so that every access below stays a shared-memory access
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t bars = smem_u32(smem + C::BAR_OFF);          // [kWW][kWS], then the query's
     const uint32_t bar_q = bars + C::NSLOT * 8;
     float *kb_s = reinterpret_cast<float *>(smem + C::KB_OFF);
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
     float *psr = reinterpret_cast<float *>(smem + C::PSR_OFF);
+    constexpr int kSBlk = C::SBLK;
     __shared__ int s_seq;
     __shared__ int s_timeout;
 
@@ -185,7 +212,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     int lo, hi;
     split_range(len, a.n_splits, split, lo, hi);
     // this warp's blocks: a contiguous run [wb0, wb0 + my_nb) of the split's
-    // 16-token blocks, streamed two to a ring stage
+    // 16-token blocks, streamed kSBlk to a ring stage
     const int nb = (int)ceil_div(hi - lo, kBlk);
     const int wb0 = (warp * nb) / kWW;
     const int my_nb = ((warp + 1) * nb) / kWW - wb0;
@@ -194,28 +221,34 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
     const uint8_t *vsc = reinterpret_cast<const uint8_t *>(a.v.sc);
     const uint32_t slot0 = (uint32_t)warp * kWS;
-    const uint32_t k_ring = smem_u32(smem + C::K_OFF) + slot0 * C::CB;     // this warp's stages
-    const uint32_t v_ring = smem_u32(smem + C::V_OFF) + slot0 * C::CB;
-    const uint32_t ks_ring = smem_u32(smem + C::KS_OFF) + slot0 * C::SB;
-    const uint32_t vs_ring = smem_u32(smem + C::VS_OFF) + slot0 * C::SB;
+    const uint32_t k_ring = smem_u32(smem + C::K_OFF) + slot0 * C::CBK;    // this warp's stages
+    const uint32_t v_ring = smem_u32(smem + C::V_OFF) + slot0 * C::CBV;
+    const uint32_t ks_ring = smem_u32(smem + C::KS_OFF) + slot0 * C::SBK;
+    const uint32_t vs_ring = smem_u32(smem + C::VS_OFF) + slot0 * C::SBV;
     const uint32_t bar_ring = bars + 8 * slot0;
 
     // lane 0 fills (and refills) the warp's stages in order; the cache is read
-    // once per call, so evict-first in L2.  A stage's codes are one 32-row box
-    // (rows past the warp's run are read and ignored; past the plane they read
-    // as zero); its scales are copied for the blocks the stage holds only, as a
-    // bulk copy has no bound of its own.
+    // once per call, so evict-first in L2.  A stage's codes are one box of
+    // kSBlk * 16 rows per plane (two side by side for 256-byte K rows; rows past
+    // the warp's run are read and ignored, past the plane they read as zero);
+    // its scales are copied for the blocks the stage holds only, as a bulk copy
+    // has no bound of its own.
     int n_issued = 0, iss_slot = 0;
     int iss_row = (int)(plane_row + lo) + kBlk * wb0;      // the next stage's first plane row
     const uint64_t pol = evict_first_policy();
     auto issue = [&]() {
         const uint32_t bar = bar_ring + 8 * (uint32_t)iss_slot;
-        const uint32_t sbytes = (uint32_t)(min(kSBlk, my_nb - kSBlk * n_issued) * C::SBB);
-        mbar_expect_tx(bar, (uint32_t)(2 * C::CB) + 2 * sbytes);
-        tma_load_2d(k_ring + (uint32_t)iss_slot * C::CB, &tmk, 0, iss_row, bar, pol);
-        tma_load_2d(v_ring + (uint32_t)iss_slot * C::CB, &tmv, 0, iss_row, bar, pol);
-        bulk_load_hint(ks_ring + (uint32_t)iss_slot * C::SB, ksc + (int64_t)iss_row * (NG * 2), sbytes, bar, pol);
-        bulk_load_hint(vs_ring + (uint32_t)iss_slot * C::SB, vsc + (int64_t)iss_row * (NG * 2), sbytes, bar, pol);
+        const uint32_t nbl = (uint32_t)min(kSBlk, my_nb - kSBlk * n_issued);
+        mbar_expect_tx(bar, (uint32_t)(C::CBK + C::CBV) + nbl * (uint32_t)(C::SBKB + C::SBVB));
+#pragma unroll
+        for (int bx = 0; bx < C::KNB; ++bx)
+            tma_load_2d(k_ring + (uint32_t)iss_slot * C::CBK + (uint32_t)(bx * C::ST * C::KBI), &tmk, bx * C::KBI,
+                        iss_row, bar, pol);
+        tma_load_2d(v_ring + (uint32_t)iss_slot * C::CBV, &tmv, 0, iss_row, bar, pol);
+        bulk_load_hint(ks_ring + (uint32_t)iss_slot * C::SBK, ksc + (int64_t)iss_row * (NGK * 2), nbl * C::SBKB, bar,
+                       pol);
+        bulk_load_hint(vs_ring + (uint32_t)iss_slot * C::SBV, vsc + (int64_t)iss_row * (NGV * 2), nbl * C::SBVB, bar,
+                       pol);
         ++n_issued;
         iss_row += kBlk * kSBlk;
         iss_slot = (iss_slot + 1 == kWS) ? 0 : iss_slot + 1;
@@ -228,10 +261,19 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     // (the same answer in every thread, so the warps' loops stay uniform)
     const bool q_ok = __syncthreads_and(mbar_wait(bar_q, 0)) != 0;
     if (!q_ok && threadIdx.x == 0) s_timeout = 1;
-    prep_query<KVQ_CODEC_Q4_G64, D, kWRows, C::NTH>(reinterpret_cast<const QT *>(smem + C::QST_OFF),
+    prep_query<KC, D, kWRows, C::NTH>(reinterpret_cast<const QT *>(smem + C::QST_OFF),
                                                      smem + C::QP_OFF, smem + C::QPL_OFF, kb_s, R, q_ok);
     __syncthreads();
     if (lane == 0 && n_st > 1) issue();
+    if constexpr (K8) {
+        // accumulator inputs of the K groups' first MMAs in C-fragment order
+        float *kbd = reinterpret_cast<float *>(smem + C::KBD_OFF);
+        for (int i = threadIdx.x; i < NGK * 16; i += C::NTH) {
+            const int g = i >> 4, t = (i >> 2) & 3, c = i & 3;
+            kbd[i] = kb_s[g * kWRows + 2 * t + (c & 1)];
+        }
+        __syncthreads();
+    }
 
     // rows 2 tig and 2 tig + 1 of this lane's accumulator columns: visible keys
     // (padding rows see everything; their results are never written)
@@ -244,11 +286,13 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     const int nv_all = len + a.causal_extra - a.n_q + 1;           // the fewest any row sees
     const float sl2 = a.scale_log2;
     // accumulator inputs of each group's first K MMA (minus the bias terms of
-    // rows 2 tig, 2 tig + 1, in the C-fragment order), and the all-ones A
-    // operand: four registers each, made distinct so that they stay in place
-    float kbv[NG][4];
+    // rows 2 tig, 2 tig + 1, in the C-fragment order; 4-bit K: four registers per
+    // group; q8_0 K, with twice the groups, reads them from shared memory), and
+    // the all-ones A operand: made distinct registers so that they stay in place
+    constexpr int NKBV = K8 ? 1 : NGK;
+    float kbv[NKBV][4];
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
+    for (int g = 0; g < NKBV; ++g) {
         const float2 b = *reinterpret_cast<const float2 *>(kb_s + g * kWRows + 2 * tig);
         asm volatile("mov.b32 %0, %1;" : "=f"(kbv[g][0]) : "f"(b.x));
         asm volatile("mov.b32 %0, %1;" : "=f"(kbv[g][1]) : "f"(b.y));
@@ -258,27 +302,28 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     uint32_t ones[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(ones[c]));   // fp16x2 (1, 1)
-    // per-lane ldmatrix offsets within a stage.  With 128-byte rows the chunk
-    // index of a group's pair is swizzled by XOR with the row's low bits, so
-    // group g's offset is the group-0 offset XOR 32 g (the XOR only touches
-    // bits 5-6 for D = 256; narrower rows use one box per chunk pair anyway).
+    // per-lane ldmatrix offsets within a stage.  A box's 16-byte chunk index is
+    // swizzled by XOR with the row's low bits, so the chunk pair u of a row
+    // (u = 0, 1, ...) lies at the pair-0 offset XOR 32 (u % pairs per box) in
+    // box u / pairs per box (the XOR only touches bits 5-6).
     const int ktok = (lane & 7) + 8 * ((lane >> 3) & 1), kch = lane >> 4;
     const int vtok = (lane & 7) + 8 * (lane >> 4), vch = (lane >> 3) & 1;
-    const uint32_t k_off0 = TG::chunk_addr(0, ktok, kch), v_off0 = TG::chunk_addr(0, vtok, vch);
+    const uint32_t k_off0 = KG::chunk_addr(0, ktok, kch), v_off0 = VG::chunk_addr(0, vtok, vch);
+    constexpr int KPPB = C::KBI / 32, VPPB = C::VRB / 32 > 0 ? C::VRB / 32 : 1;   // chunk pairs per box
     // query B fragments: chunk 8 g + 4 kp + (lane >> 3) of row lane & 7, swizzled by
     // XOR with the row: the kp = 0 and kp = 1 addresses, group g at + 128 g
     const uint32_t qp_base = smem_u32(smem + C::QP_OFF), qpl_base = smem_u32(smem + C::QPL_OFF);
     const uint32_t q_row = (uint32_t)((lane & 7) * D * 2), q_sw = (uint32_t)(lane & 7), q_ch = (uint32_t)(lane >> 3);
     const uint32_t qa0 = q_row + ((q_ch ^ q_sw) << 4), qa1 = q_row + (((4u + q_ch) ^ q_sw) << 4);
 
-    float o[4 * NG][4];          // O^T, m-tile 4 g + 2 lc + j: chunk 2 g + lc, nibble pairs 2 j / 2 j + 1
-    float ps[NG][4];             // sum over tokens of P' per group (all accumulator rows equal)
+    float o[4 * NGV][4];         // O^T, m-tile 4 g + 2 lc + j: chunk 2 g + lc, nibble pairs 2 j / 2 j + 1
+    float ps[NGV][4];            // sum over tokens of P' per V group (all accumulator rows equal)
 #pragma unroll
-    for (int t = 0; t < 4 * NG; ++t)
+    for (int t = 0; t < 4 * NGV; ++t)
 #pragma unroll
         for (int c = 0; c < 4; ++c) o[t][c] = 0.0f;
 #pragma unroll
-    for (int g = 0; g < NG; ++g)
+    for (int g = 0; g < NGV; ++g)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ps[g][c] = 0.0f;
     // running reference maximum (log2 units) and sum of rows 2 tig, 2 tig + 1.
@@ -305,39 +350,57 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         const int nbl = min(kSBlk, my_nb - kSBlk * j);
 #pragma unroll 1
         for (int b = 0; b < nbl; ++b, t0 += kBlk) {
-        const uint32_t kb_addr = k_ring + (uint32_t)slot * C::CB + (uint32_t)b * C::CBB + k_off0;
-        const uint32_t vb_addr = v_ring + (uint32_t)slot * C::CB + (uint32_t)b * C::CBB + v_off0;
-        const uint32_t ksa = ks_ring + (uint32_t)slot * C::SB + (uint32_t)b * C::SBB + (uint32_t)gid * (NG * 2);
-        const uint32_t vsa = vs_ring + (uint32_t)slot * C::SB + (uint32_t)b * C::SBB + (uint32_t)gid * (NG * 2);
+        const uint32_t kb_addr = k_ring + (uint32_t)slot * C::CBK + (uint32_t)(b * kBlk * C::KBI) + k_off0;
+        const uint32_t vb_addr = v_ring + (uint32_t)slot * C::CBV + (uint32_t)(b * kBlk * C::VRB) + v_off0;
+        const uint32_t ksa = ks_ring + (uint32_t)slot * C::SBK + (uint32_t)(b * C::SBKB) + (uint32_t)gid * (NGK * 2);
+        const uint32_t vsa = vs_ring + (uint32_t)slot * C::SBV + (uint32_t)(b * C::SBVB) + (uint32_t)gid * (NGV * 2);
         const bool edge = (t0 + kBlk > hi) || (t0 + kBlk > nv_all);
 
         // ---- S^T = K Q^T: tokens gid, gid + 8 (rows of the fragment) x rows 2 tig, 2 tig + 1
-        uint32_t kw0[(NG + 1) / 2], kw1[(NG + 1) / 2];
-        lds_scales<NG>(ksa, kw0);
-        lds_scales<NG>(ksa + 8 * (NG * 2), kw1);
-        float sk0[NG], sk1[NG];
-        scales_to_float<NG>(kw0, sk0);
-        scales_to_float<NG>(kw1, sk1);
+        uint32_t kw0[(NGK + 1) / 2], kw1[(NGK + 1) / 2];
+        lds_scales<NGK>(ksa, kw0);
+        lds_scales<NGK>(ksa + 8 * (NGK * 2), kw1);
+        float sk0[NGK], sk1[NGK];
+        scales_to_float<NGK>(kw0, sk0);
+        scales_to_float<NGK>(kw1, sk1);
         float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
+        for (int g = 0; g < NGK; ++g) {
+            // K group g is the row's chunk pair g: one ldmatrix, KSTEPS_G k-steps
             uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb_addr ^ (uint32_t)(32 * g), r0, r1, r2, r3);
+            ldsm_x4((kb_addr ^ (uint32_t)(32 * (g % KPPB))) + (uint32_t)((g / KPPB) * C::ST * C::KBI), r0, r1, r2, r3);
             uint32_t h0[4], h1[4], h2[4], h3[4];
-            unpack_q4_biased(r0, h0);
-            unpack_q4_biased(r1, h1);
-            unpack_q4_biased(r2, h2);
-            unpack_q4_biased(r3, h3);
+            if constexpr (K8) {
+                uint32_t t2[2];
+                unpack_q8_biased(r0, t2); h0[0] = t2[0]; h0[1] = t2[1];
+                unpack_q8_biased(r1, t2); h1[0] = t2[0]; h1[1] = t2[1];
+                unpack_q8_biased(r2, t2); h2[0] = t2[0]; h2[1] = t2[1];
+                unpack_q8_biased(r3, t2); h3[0] = t2[0]; h3[1] = t2[1];
+            } else {
+                unpack_q4_biased(r0, h0);
+                unpack_q4_biased(r1, h1);
+                unpack_q4_biased(r2, h2);
+                unpack_q4_biased(r3, h3);
+            }
+            float c0, c1, c2, c3;
+            if constexpr (K8) {
+                const uint4 kbq = lds128(smem_u32(smem + C::KBD_OFF) + (uint32_t)(g * 64 + tig * 16));
+                c0 = __uint_as_float(kbq.x); c1 = __uint_as_float(kbq.y);
+                c2 = __uint_as_float(kbq.z); c3 = __uint_as_float(kbq.w);
+            } else {
+                c0 = kbv[g % NKBV][0]; c1 = kbv[g % NKBV][1]; c2 = kbv[g % NKBV][2]; c3 = kbv[g % NKBV][3];
+            }
             float cg[4];
 #pragma unroll
-            for (int kp = 0; kp < 2; ++kp) {
-                // B fragments of k-steps 4 g + 2 kp and 4 g + 2 kp + 1 in one ldmatrix
-                const uint32_t qa = (kp ? qa1 : qa0) + (uint32_t)(128 * g);
+            for (int kp = 0; kp < C::KSTEPS_G / 2; ++kp) {
+                // B fragments of k-steps 2 p and 2 p + 1 (p = the group's pair kp) in one ldmatrix
+                const int p = g * (C::KSTEPS_G / 2) + kp;
+                const uint32_t qa = ((p & 1) ? qa1 : qa0) + (uint32_t)(128 * (p >> 1));
                 uint32_t b00, b01, b10, b11;
                 ldsm_x4(qp_base + qa, b00, b01, b10, b11);
                 const int k = 2 * kp;
                 if (kp == 0)
-                    mma16816_c(cg, h0[k], h1[k], h2[k], h3[k], b00, b01, kbv[g][0], kbv[g][1], kbv[g][2], kbv[g][3]);
+                    mma16816_c(cg, h0[k], h1[k], h2[k], h3[k], b00, b01, c0, c1, c2, c3);
                 else
                     mma16816(cg, h0[k], h1[k], h2[k], h3[k], b00, b01);
                 mma16816(cg, h0[k + 1], h1[k + 1], h2[k + 1], h3[k + 1], b10, b11);
@@ -357,19 +420,19 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
 
         // V scales of tokens gid, gid + 8 (0 past the split end, where the plane
         // may hold anything)
-        uint32_t vw0[(NG + 1) / 2], vw1[(NG + 1) / 2];
-        lds_scales<NG>(vsa, vw0);
-        lds_scales<NG>(vsa + 8 * (NG * 2), vw1);
+        uint32_t vw0[(NGV + 1) / 2], vw1[(NGV + 1) / 2];
+        lds_scales<NGV>(vsa, vw0);
+        lds_scales<NGV>(vsa + 8 * (NGV * 2), vw1);
         // some V scale of the lane's tokens is 256 or more: a non-negative fp16
         // half h is >= 256 (0x5C00) exactly when h + 0x2400 reaches bit 15 (no
         // carry crosses into the other half); garbage past the split end only
         // makes this answer yes, which is safe
         uint32_t vge = (vw0[0] + 0x24002400u) | (vw1[0] + 0x24002400u);
-        if constexpr (NG == 4) vge |= (vw0[1] + 0x24002400u) | (vw1[1] + 0x24002400u);
+        if constexpr (NGV == 4) vge |= (vw0[1] + 0x24002400u) | (vw1[1] + 0x24002400u);
         const bool big = (vge & 0x80008000u) != 0u;
-        float sv0[NG], sv1[NG];
-        scales_to_float<NG>(vw0, sv0);
-        scales_to_float<NG>(vw1, sv1);
+        float sv0[NGV], sv1[NGV];
+        scales_to_float<NGV>(vw0, sv0);
+        scales_to_float<NGV>(vw1, sv1);
         if (edge) {
             const int ta = t0 + gid, tc = ta + 8;
             sc[0] = (ta < hi && ta < nv0) ? sc[0] : -INFINITY;
@@ -377,7 +440,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
             sc[2] = (tc < hi && tc < nv0) ? sc[2] : -INFINITY;
             sc[3] = (tc < hi && tc < nv1) ? sc[3] : -INFINITY;
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
+            for (int g = 0; g < NGV; ++g) {
                 sv0[g] = ta < hi ? sv0[g] : 0.0f;
                 sv1[g] = tc < hi ? sv1[g] : 0.0f;
             }
@@ -398,14 +461,14 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
                 const float c0 = (n0 == -INFINITY) ? 1.0f : ex2(m0 - n0);
                 const float c1 = (n1 == -INFINITY) ? 1.0f : ex2(m1 - n1);
 #pragma unroll
-                for (int t = 0; t < 4 * NG; ++t) {
+                for (int t = 0; t < 4 * NGV; ++t) {
                     o[t][0] *= c0;
                     o[t][1] *= c1;
                     o[t][2] *= c0;
                     o[t][3] *= c1;
                 }
 #pragma unroll
-                for (int g = 0; g < NG; ++g) {
+                for (int g = 0; g < NGV; ++g) {
                     ps[g][0] *= c0;
                     ps[g][1] *= c1;
                     ps[g][2] *= c0;
@@ -424,13 +487,13 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
 
         // ---- O^T += V^T P'^T per V group
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
+        for (int g = 0; g < NGV; ++g) {
             // P' of tokens gid (rows 2 tig, 2 tig + 1) and gid + 8, transposed to
             // tokens (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9) of row gid
             const uint32_t pb0 = movmatrix_t(pack_f16x2(p0 * sv0[g], p1 * sv0[g]));
             const uint32_t pb1 = movmatrix_t(pack_f16x2(p2 * sv1[g], p3 * sv1[g]));
             uint32_t rv0, rv1, rv2, rv3;     // tokens 0-7 chunks 2g, 2g+1; tokens 8-15 chunks 2g, 2g+1
-            ldsm_x4_t(vb_addr ^ (uint32_t)(32 * g), rv0, rv1, rv2, rv3);
+            ldsm_x4_t(vb_addr ^ (uint32_t)(32 * (g % VPPB)), rv0, rv1, rv2, rv3);
 #pragma unroll
             for (int lc = 0; lc < 2; ++lc) {
                 const uint32_t ra = lc ? rv1 : rv0, rb = lc ? rv3 : rv2;
@@ -483,14 +546,14 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         red[warp * 16 + 8 + 2 * tig] = l0;
         red[warp * 16 + 8 + 2 * tig + 1] = l1;
 #pragma unroll
-        for (int g = 0; g < NG; ++g)
-            *reinterpret_cast<float2 *>(psr + (warp * NG + g) * 8 + 2 * tig) = make_float2(ps[g][0], ps[g][1]);
+        for (int g = 0; g < NGV; ++g)
+            *reinterpret_cast<float2 *>(psr + (warp * NGV + g) * 8 + 2 * tig) = make_float2(ps[g][0], ps[g][1]);
     }
     {
         float *cb = reinterpret_cast<float *>(smem + C::K_OFF) + warp * (kWRows * D);
         const bool w0 = 2 * tig < R, w1 = 2 * tig + 1 < R;     // padding rows are never read
 #pragma unroll
-        for (int t = 0; t < 4 * NG; ++t) {
+        for (int t = 0; t < 4 * NGV; ++t) {
             const int d = 32 * (t >> 1) + 4 * gid + 2 * (t & 1);
             if (w0) *reinterpret_cast<float2 *>(cb + (2 * tig) * D + d) = make_float2(o[t][0], o[t][2]);
             if (w1) *reinterpret_cast<float2 *>(cb + (2 * tig + 1) * D + d) = make_float2(o[t][1], o[t][3]);
@@ -514,7 +577,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
                 const float mw = red[w * 16 + r];
                 const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
                 L = fmaf(f, red[w * 16 + 8 + r], L);
-                P = fmaf(f, psr[(w * NG + g) * 8 + r], P);
+                P = fmaf(f, psr[(w * NGV + g) * 8 + r], P);
                 const float4 v = *reinterpret_cast<const float4 *>(cb0 + (w * kWRows + r) * D + d);
                 acc.x = fmaf(f, v.x, acc.x);
                 acc.y = fmaf(f, v.y, acc.y);
@@ -548,16 +611,16 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int D, typename QT>
+template <int KC, int D, typename QT>
 cudaError_t warp_prepare(int *per_sm)
 {
-    using C = WCfg<D, QT>;
+    using C = WCfg<KC, D, QT>;
     static PerDevice pd;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int n = per_device(pd, dev, []() -> int {
-        auto kern = decode_warp_kernel<D, QT>;
+        auto kern = decode_warp_kernel<KC, D, QT>;
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (r != cudaSuccess) return -(int)r;
         int v = 0;
@@ -570,49 +633,65 @@ cudaError_t warp_prepare(int *per_sm)
     return cudaSuccess;
 }
 
-template <int D, typename QT>
+template <int KC, int D, typename QT>
 cudaError_t warp_launch(const DecodeArgs &a, cudaStream_t st)
 {
-    using C = WCfg<D, QT>;
+    using C = WCfg<KC, D, QT>;
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
     CUtensorMap tk, tv;
-    if (!make_codes_map(&tk, a.k.qs, C::RB, rows, kBlk * kSBlk) ||
-        !make_codes_map(&tv, a.v.qs, C::RB, rows, kBlk * kSBlk))
+    if (!make_codes_map(&tk, a.k.qs, C::KRB, rows, C::ST) || !make_codes_map(&tv, a.v.qs, C::VRB, rows, C::ST))
         return cudaErrorInvalidValue;
     int per_sm = 0;
-    cudaError_t e = warp_prepare<D, QT>(&per_sm);
+    cudaError_t e = warp_prepare<KC, D, QT>(&per_sm);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
-    return launch_pdl(decode_warp_kernel<D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv);
+    return launch_pdl(decode_warp_kernel<KC, D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv);
 }
 
-template <int D>
+template <int KC, int D>
 int warp_per_sm()
 {
     int n = 0;
-    if (warp_prepare<D, __half>(&n) != cudaSuccess) {
+    if (warp_prepare<KC, D, __half>(&n) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     return n;
 }
 
+template <int KC>
+int warp_per_sm_d(int head_dim)
+{
+    switch (head_dim) {
+    case 64: return warp_per_sm<KC, 64>();
+    case 128: return warp_per_sm<KC, 128>();
+    case 256: return warp_per_sm<KC, 256>();
+    default: return 0;
+    }
+}
+
+template <int KC>
+cudaError_t warp_launch_d(const DecodeArgs &a, bool f16, cudaStream_t st)
+{
+    switch (a.head_dim) {
+    case 64: return f16 ? warp_launch<KC, 64, __half>(a, st) : warp_launch<KC, 64, float>(a, st);
+    case 128: return f16 ? warp_launch<KC, 128, __half>(a, st) : warp_launch<KC, 128, float>(a, st);
+    case 256: return f16 ? warp_launch<KC, 256, __half>(a, st) : warp_launch<KC, 256, float>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 bool decode_warp_shape(int k_codec, int v_codec, int head_dim, int rows_per_kv_head)
 {
-    return k_codec == KVQ_CODEC_Q4_G64 && v_codec == KVQ_CODEC_Q4_G64 && rows_per_kv_head >= 1 &&
-           rows_per_kv_head <= kWRows && (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    return (k_codec == KVQ_CODEC_Q4_G64 || k_codec == KVQ_CODEC_Q8_0) && v_codec == KVQ_CODEC_Q4_G64 &&
+           rows_per_kv_head >= 1 && rows_per_kv_head <= kWRows && (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
 
-int decode_warp_ctas_per_sm(int head_dim)
+int decode_warp_ctas_per_sm(int k_codec, int head_dim)
 {
-    switch (head_dim) {
-    case 64: return warp_per_sm<64>();
-    case 128: return warp_per_sm<128>();
-    case 256: return warp_per_sm<256>();
-    default: return 0;
-    }
+    return k_codec == KVQ_CODEC_Q8_0 ? warp_per_sm_d<KVQ_CODEC_Q8_0>(head_dim) : warp_per_sm_d<KVQ_CODEC_Q4_G64>(head_dim);
 }
 
 bool decode_warp_takes(const DecodeArgs &a)
@@ -620,18 +699,14 @@ bool decode_warp_takes(const DecodeArgs &a)
     const int R = a.n_q * (a.n_heads / a.n_kv_heads);
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
     return decode_warp_shape(a.k.codec, a.v.codec, a.head_dim, R) && rows < (1LL << 31) &&
-           tensor_maps_available() && decode_warp_ctas_per_sm(a.head_dim) > 0;
+           tensor_maps_available() && decode_warp_ctas_per_sm(a.k.codec, a.head_dim) > 0;
 }
 
 cudaError_t launch_decode_warp(const DecodeArgs &a, int q_dtype, cudaStream_t st)
 {
     const bool f16 = q_dtype == KVQ_F16;
-    switch (a.head_dim) {
-    case 64: return f16 ? warp_launch<64, __half>(a, st) : warp_launch<64, float>(a, st);
-    case 128: return f16 ? warp_launch<128, __half>(a, st) : warp_launch<128, float>(a, st);
-    case 256: return f16 ? warp_launch<256, __half>(a, st) : warp_launch<256, float>(a, st);
-    default: return cudaErrorInvalidValue;
-    }
+    return a.k.codec == KVQ_CODEC_Q8_0 ? warp_launch_d<KVQ_CODEC_Q8_0>(a, f16, st)
+                                       : warp_launch_d<KVQ_CODEC_Q4_G64>(a, f16, st);
 }
 
 }  // namespace kvq

@@ -199,13 +199,13 @@ cudaError_t launch_decode_tc_q8v(const DecodeArgs &a, int q_dtype, cudaStream_t 
 int decode_tc_q8v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 cudaError_t launch_decode_tc_fp4v(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 int decode_tc_fp4v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
-// Up to 8 query rows per kv head over Q4_G64 K and V (head_dim 64/128/256):
+// Up to 8 query rows per kv head over Q4_G64 or q8_0 K and Q4_G64 V (head_dim 64/128/256):
 // CTAs of warps that each own whole 16-token blocks (kvq_decode_warp.cu).
 // decode_warp_shape: the shapes it takes (also for the split policy);
 // decode_warp_takes: it runs these arguments.
 bool decode_warp_shape(int k_codec, int v_codec, int head_dim, int rows_per_kv_head);
 bool decode_warp_takes(const DecodeArgs &a);
-int decode_warp_ctas_per_sm(int head_dim);
+int decode_warp_ctas_per_sm(int k_codec, int head_dim);
 cudaError_t launch_decode_warp(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // Prompt-chunk path on the fifth-generation tensor cores (tcgen05): blocks of
 // 128 query rows per CTA, Q4_G64 K and V, head_dim 64/128/256,
