@@ -1,23 +1,28 @@
-// kvq_decode_warp.cu -- split-K decode attention over a Q4_G64 cache for up to
-// 8 query rows per kv head (a GQA group of one token, or 1 + k MTP tokens of
-// a narrow group): one CTA of 12 warps per SM, each warp owning whole blocks
-// of 16 tokens over all of head_dim.
+// kvq_decode_warp.cu -- split-K decode attention for up to 8 query rows per
+// kv head (a GQA group of one token, or 1 + k MTP tokens of a narrow group)
+// over a Q4_G64 V plane and a Q4_G64 or q8_0 K plane: one CTA of 12 warps per
+// SM, each warp owning whole blocks of 16 tokens over all of head_dim.
 // (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
-// this fork is": 4-bit signed codes sharing one fp16 scale per 64 values.)
+// this fork is": 4-bit signed codes sharing one fp16 scale per 64 values, and
+// the q8_0 K / Q4_G64 V pair.)
 //
-// Per (sequence, kv head, split) the split's tokens are cut into blocks of 16;
-// warp w takes blocks w, w + 12, w + 24, ...  Every warp streams its own
-// blocks through its own ring of shared-memory stages (K and V codes by 2D
-// TMA, 16 rows a box; their fp16 scales by bulk copies) and keeps its own
-// online-softmax state, so nothing in the loop waits on another warp.  Per
-// block the warp:
+// Per (sequence, kv head, split) the split's tokens are cut into blocks of 16
+// and each warp takes a contiguous run of them, streamed through its own ring
+// of two shared-memory stages (K and V codes by 2D TMA, 32 rows a box for
+// 4-bit K, 16 for q8_0 K, whose rows take two 128-byte boxes; the fp16 scales
+// by bulk copies).  Each warp keeps its own online-softmax state, so nothing
+// in the loop waits on another warp.  Per block the warp:
 //  * computes S^T = K Q^T (tokens on M, query rows on N) on mma.sync.m16n8k16:
-//    the K codes enter as exact fp16 integers with their bias (1032 + q, or
-//    1152 + 16 q at odd head_dim indices; one LOP3 per two values), each
-//    64-value group in its own accumulator that starts at minus the group's
-//    bias term and is then scaled by the token's fp16 scale in fp32;
-//  * takes the block's per-row maximum with three shuffles, rescales its O and
-//    sums only when a row maximum grew (a warp vote), and forms p = 2^(s - m);
+//    the K codes enter as exact fp16 integers with their bias (4-bit: 1032 + q,
+//    or 1152 + 16 q at odd head_dim indices, one LOP3 per two values; q8_0:
+//    1152 + q, one PRMT per two values), each scale group in its own
+//    accumulator that starts at minus the group's bias term and is then
+//    scaled by the token's fp16 scale in fp32;
+//  * takes the block's per-row maximum with three shuffles and forms
+//    p = 2^(s - m) against a running reference m that is raised (with O and
+//    the sums rescaled) only when a block's maximum passes it by more than 2^8,
+//    or by anything while a V scale of the block is 256 or more, so P' below
+//    stays a finite fp16 value;
 //  * forms P' = p * v_scale(token, group) in fp32, rounds it once to fp16 and
 //    transposes the 8x8 fp16 fragments with movmatrix into the B operand of
 //    O^T += V^T P'^T (so every exponential is computed once and no score goes
@@ -27,9 +32,10 @@
 //    (q + 8) 2^-24 (16 (q + 8) 2^-24 at odd indices), one LOP3 per two values;
 //    the offset 8 is removed at the end from the sum of P' per group, which
 //    one MMA against an all-ones operand accumulates per block.
-// At the end the warps' (maximum, sum, O) are combined through shared memory
-// (the rings are free by then) and the CTA writes its normalised result (one
-// split) or its partial with the log-sum-exp.
+// At the end each warp leaves its (reference, sum, sums of P', raw O^T) in
+// shared memory (O^T over its own K ring), and after one barrier every thread
+// forms whole outputs of the CTA: its normalised result (one split) or its
+// partial with the log-sum-exp for the merge kernel.
 //
 // Every mbarrier wait is bounded: after ~1 s the warp stops waiting, the CTA
 // sets KVQ_ERR_TIMEOUT in the caller's error word and finishes; nothing traps.
@@ -142,7 +148,8 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
 
 template <int KC, int D, typename QT>
 __global__ void __launch_bounds__(kWW * 32, kWMinBlocks)
-decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv)
+decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmk1, const __grid_constant__ CUtensorMap tmv1)
 {
     using C = WCfg<KC, D, QT>;
     constexpr int NGK = C::NGK, NGV = C::NGV;
@@ -171,6 +178,10 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+        if constexpr (C::SBLK > 1) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk1)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv1)) : "memory");
+        }
         s_timeout = 0;
         for (int i = 0; i <= C::NSLOT; ++i) mbar_init(bars + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -229,22 +240,23 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
 
     // lane 0 fills (and refills) the warp's stages in order; the cache is read
     // once per call, so evict-first in L2.  A stage's codes are one box of
-    // kSBlk * 16 rows per plane (two side by side for 256-byte K rows; rows past
-    // the warp's run are read and ignored, past the plane they read as zero);
-    // its scales are copied for the blocks the stage holds only, as a bulk copy
-    // has no bound of its own.
+    // kSBlk * 16 rows per plane (two side by side for 256-byte K rows), a box
+    // of 16 rows (maps tmk1, tmv1) for a run's odd last block; the scales are
+    // copied for the blocks the stage holds.
     int n_issued = 0, iss_slot = 0;
     int iss_row = (int)(plane_row + lo) + kBlk * wb0;      // the next stage's first plane row
     const uint64_t pol = evict_first_policy();
     auto issue = [&]() {
         const uint32_t bar = bar_ring + 8 * (uint32_t)iss_slot;
         const uint32_t nbl = (uint32_t)min(kSBlk, my_nb - kSBlk * n_issued);
-        mbar_expect_tx(bar, (uint32_t)(C::CBK + C::CBV) + nbl * (uint32_t)(C::SBKB + C::SBVB));
+        const bool full = (nbl == (uint32_t)kSBlk);
+        const CUtensorMap *mk = full ? &tmk : &tmk1, *mv = full ? &tmv : &tmv1;
+        mbar_expect_tx(bar, nbl * (uint32_t)(kBlk * (C::KRB + C::VRB) + C::SBKB + C::SBVB));
 #pragma unroll
         for (int bx = 0; bx < C::KNB; ++bx)
-            tma_load_2d(k_ring + (uint32_t)iss_slot * C::CBK + (uint32_t)(bx * C::ST * C::KBI), &tmk, bx * C::KBI,
+            tma_load_2d(k_ring + (uint32_t)iss_slot * C::CBK + (uint32_t)(bx * C::ST * C::KBI), mk, bx * C::KBI,
                         iss_row, bar, pol);
-        tma_load_2d(v_ring + (uint32_t)iss_slot * C::CBV, &tmv, 0, iss_row, bar, pol);
+        tma_load_2d(v_ring + (uint32_t)iss_slot * C::CBV, mv, 0, iss_row, bar, pol);
         bulk_load_hint(ks_ring + (uint32_t)iss_slot * C::SBK, ksc + (int64_t)iss_row * (NGK * 2), nbl * C::SBKB, bar,
                        pol);
         bulk_load_hint(vs_ring + (uint32_t)iss_slot * C::SBV, vsc + (int64_t)iss_row * (NGV * 2), nbl * C::SBVB, bar,
@@ -638,14 +650,16 @@ cudaError_t warp_launch(const DecodeArgs &a, cudaStream_t st)
 {
     using C = WCfg<KC, D, QT>;
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
-    CUtensorMap tk, tv;
-    if (!make_codes_map(&tk, a.k.qs, C::KRB, rows, C::ST) || !make_codes_map(&tv, a.v.qs, C::VRB, rows, C::ST))
+    // boxes of a whole stage, and of one block (a run's odd last block)
+    CUtensorMap tk, tv, tk1, tv1;
+    if (!make_codes_map(&tk, a.k.qs, C::KRB, rows, C::ST) || !make_codes_map(&tv, a.v.qs, C::VRB, rows, C::ST) ||
+        !make_codes_map(&tk1, a.k.qs, C::KRB, rows, kBlk) || !make_codes_map(&tv1, a.v.qs, C::VRB, rows, kBlk))
         return cudaErrorInvalidValue;
     int per_sm = 0;
     cudaError_t e = warp_prepare<KC, D, QT>(&per_sm);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
-    return launch_pdl(decode_warp_kernel<KC, D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv);
+    return launch_pdl(decode_warp_kernel<KC, D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv, tk1, tv1);
 }
 
 template <int KC, int D>
