@@ -146,9 +146,11 @@ kvq_status kvq_quantize_append(const kvq_cache *k, const kvq_cache *v,
 
 /* Split count kvq_decode_attention uses for n_splits = 0 with these caches and
  * arguments on the current device.  One sequence: one wave of the decode
- * kernel's CTAs (how many fit on an SM depends on the K codec, head_dim and the
- * query rows per kv head); a batch, whose lengths may be ragged: up to four
- * waves' worth at three CTAs per SM.  Never fewer than 256 keys per split.
+ * kernel's CTAs (which kernel runs, and how many of its CTAs fit on an SM,
+ * depends on the codecs, head_dim and the query rows per kv head: one CTA per
+ * SM for up to 8 rows over Q4_G64 V, two or three otherwise); a batch, whose
+ * lengths may be ragged: up to four waves' worth.  Never fewer than 256 keys
+ * per split.
  * Only codec, n_seq, n_kv_heads and head_dim of k and v are read (their plane
  * pointers may be NULL).  Returns 1 for invalid arguments. */
 int32_t kvq_decode_default_splits(const kvq_cache *k, const kvq_cache *v, int32_t n_heads, int32_t n_q,
