@@ -1,5 +1,7 @@
 // kvq_decode_tc.cu -- the tensor-core decode kernel (kvq_decode_tc.cuh) for V
-// in Q4_G64, and the dispatch of the four V codecs.
+// in Q4_G64, and the dispatch of the decode kernels: prompt chunks to the
+// tcgen05 kernel, up to 8 rows per kv head over Q4_G64 V to the single-warp-
+// block kernel, everything else to kvq_decode_tc.cuh's four V-codec instances.
 #include "kvq_decode_tc.cuh"
 
 namespace kvq {

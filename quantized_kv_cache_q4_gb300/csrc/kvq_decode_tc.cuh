@@ -15,6 +15,9 @@
 // Per (sequence, kv head, split) the query rows of the kv head attend to the
 // split's tokens intersected with each row's visible keys; the result is final
 // (one split) or a partial normalised over the split with its log-sum-exp.
+// Shapes of up to 8 rows per kv head over Q4_G64 V with Q4_G64 or q8_0 K go to
+// the single-warp-block kernel of kvq_decode_warp.cu instead; this kernel takes
+// the rest (MTP verify with more rows, the other V codecs, NVFP4 or Q4_G32 K).
 //
 // Work of one CTA (four warps, no dedicated producer), one CTA barrier per tile:
 //  * Thread 0 fetches the query rows with 1D bulk copies and the first tiles of
