@@ -18,7 +18,7 @@ bool decode_tc_supported(const DecodeArgs &a)
 int decode_ctas_per_sm(int k_codec, int v_codec, int head_dim, int rows_per_kv_head)
 {
     if (rows_per_kv_head < 1) return 0;
-    if (decode_warp_shape(k_codec, v_codec, head_dim, rows_per_kv_head)) return decode_warp_ctas_per_sm(k_codec, head_dim);
+    if (decode_warp_shape(k_codec, v_codec, head_dim, rows_per_kv_head)) return decode_warp_ctas_per_sm(k_codec, v_codec, head_dim);
     const int nt = (min(rows_per_kv_head, kTcRowsPerCta) + 7) / 8;
     if (v_codec == KVQ_CODEC_Q4_G64) return per_sm_for_v<KVQ_CODEC_Q4_G64>(k_codec, head_dim, nt);
     if (v_codec == KVQ_CODEC_Q4_G32) return decode_tc_g32_ctas_per_sm(k_codec, head_dim, nt);

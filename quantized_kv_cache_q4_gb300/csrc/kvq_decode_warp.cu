@@ -51,10 +51,12 @@ constexpr int kWMinBlocks = 1;      // CTAs per SM
 constexpr int kWS = 2;              // ring stages per warp
 constexpr int kWRows = 8;           // query rows per kv head (one n-tile)
 
-template <int KC, int D, typename QT>
+template <int KC, int VC, int D, typename QT>
 struct WCfg {
     static constexpr int NGK = D / group_size(KC);    // K scale groups per row
-    static constexpr int NGV = D / 64;                // V (Q4_G64) scale groups per row
+    static constexpr int VGS = group_size(VC);        // V (4-bit) scale group: 64 or 32 values
+    static constexpr int NGV = D / VGS;               // V scale groups per row
+    static constexpr int NCP = D / 64;                // V chunk pairs per row (one ldmatrix.trans each)
     static constexpr int KRB = row_bytes(KC, D);      // code bytes per row
     static constexpr int VRB = D / 2;
     static constexpr int KBI = KRB < 128 ? KRB : 128; // K box width (bytes); K rows of 256 bytes take two boxes
@@ -146,13 +148,14 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
     return y;
 }
 
-template <int KC, int D, typename QT>
+template <int KC, int VC, int D, typename QT>
 __global__ void __launch_bounds__(kWW * 32, kWMinBlocks)
 decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmk1, const __grid_constant__ CUtensorMap tmv1)
 {
-    using C = WCfg<KC, D, QT>;
-    constexpr int NGK = C::NGK, NGV = C::NGV;
+    using C = WCfg<KC, VC, D, QT>;
+    constexpr int NGK = C::NGK, NGV = C::NGV, NCP = C::NCP;
+    constexpr bool G32V = (VC == KVQ_CODEC_Q4_G32);
     constexpr bool K8 = (KC == KVQ_CODEC_Q8_0);
     using KG = TileGeom<C::KBI>;
     using VG = TileGeom<C::VRB>;
@@ -328,10 +331,10 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     const uint32_t q_row = (uint32_t)((lane & 7) * D * 2), q_sw = (uint32_t)(lane & 7), q_ch = (uint32_t)(lane >> 3);
     const uint32_t qa0 = q_row + ((q_ch ^ q_sw) << 4), qa1 = q_row + (((4u + q_ch) ^ q_sw) << 4);
 
-    float o[4 * NGV][4];         // O^T, m-tile 4 g + 2 lc + j: chunk 2 g + lc, nibble pairs 2 j / 2 j + 1
+    float o[4 * NCP][4];         // O^T, m-tile 4 u + 2 lc + j: chunk 2 u + lc, nibble pairs 2 j / 2 j + 1
     float ps[NGV][4];            // sum over tokens of P' per V group (all accumulator rows equal)
 #pragma unroll
-    for (int t = 0; t < 4 * NGV; ++t)
+    for (int t = 0; t < 4 * NCP; ++t)
 #pragma unroll
         for (int c = 0; c < 4; ++c) o[t][c] = 0.0f;
 #pragma unroll
@@ -440,7 +443,8 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         // carry crosses into the other half); garbage past the split end only
         // makes this answer yes, which is safe
         uint32_t vge = (vw0[0] + 0x24002400u) | (vw1[0] + 0x24002400u);
-        if constexpr (NGV == 4) vge |= (vw0[1] + 0x24002400u) | (vw1[1] + 0x24002400u);
+#pragma unroll
+        for (int w = 1; w < (NGV + 1) / 2; ++w) vge |= (vw0[w] + 0x24002400u) | (vw1[w] + 0x24002400u);
         const bool big = (vge & 0x80008000u) != 0u;
         float sv0[NGV], sv1[NGV];
         scales_to_float<NGV>(vw0, sv0);
@@ -473,7 +477,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
                 const float c0 = (n0 == -INFINITY) ? 1.0f : ex2(m0 - n0);
                 const float c1 = (n1 == -INFINITY) ? 1.0f : ex2(m1 - n1);
 #pragma unroll
-                for (int t = 0; t < 4 * NGV; ++t) {
+                for (int t = 0; t < 4 * NCP; ++t) {
                     o[t][0] *= c0;
                     o[t][1] *= c1;
                     o[t][2] *= c0;
@@ -497,26 +501,32 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         l0 += p0 + p2;
         l1 += p1 + p3;
 
-        // ---- O^T += V^T P'^T per V group
+        // ---- O^T += V^T P'^T per V chunk pair (one V group for Q4_G64, two for Q4_G32)
 #pragma unroll
-        for (int g = 0; g < NGV; ++g) {
-            // P' of tokens gid (rows 2 tig, 2 tig + 1) and gid + 8, transposed to
-            // tokens (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9) of row gid
-            const uint32_t pb0 = movmatrix_t(pack_f16x2(p0 * sv0[g], p1 * sv0[g]));
-            const uint32_t pb1 = movmatrix_t(pack_f16x2(p2 * sv1[g], p3 * sv1[g]));
-            uint32_t rv0, rv1, rv2, rv3;     // tokens 0-7 chunks 2g, 2g+1; tokens 8-15 chunks 2g, 2g+1
-            ldsm_x4_t(vb_addr ^ (uint32_t)(32 * (g % VPPB)), rv0, rv1, rv2, rv3);
+        for (int u = 0; u < NCP; ++u) {
+            uint32_t rv0, rv1, rv2, rv3;     // tokens 0-7 chunks 2u, 2u+1; tokens 8-15 chunks 2u, 2u+1
+            ldsm_x4_t(vb_addr ^ (uint32_t)(32 * (u % VPPB)), rv0, rv1, rv2, rv3);
+            uint32_t pb0 = 0, pb1 = 0;
 #pragma unroll
             for (int lc = 0; lc < 2; ++lc) {
+                if (lc == 0 || G32V) {
+                    // P' of the chunk's group, tokens gid (rows 2 tig, 2 tig + 1) and
+                    // gid + 8, transposed to tokens (2 tig, 2 tig + 1) and (2 tig + 8,
+                    // 2 tig + 9) of row gid
+                    const int g = G32V ? 2 * u + lc : u;
+                    pb0 = movmatrix_t(pack_f16x2(p0 * sv0[g], p1 * sv0[g]));
+                    pb1 = movmatrix_t(pack_f16x2(p2 * sv1[g], p3 * sv1[g]));
+                }
                 const uint32_t ra = lc ? rv1 : rv0, rb = lc ? rv3 : rv2;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t a0 = q4_pair_sub(ra, 2 * j), a1 = q4_pair_sub(ra, 2 * j + 1);
                     const uint32_t a2 = q4_pair_sub(rb, 2 * j), a3 = q4_pair_sub(rb, 2 * j + 1);
-                    mma16816(o[4 * g + 2 * lc + j], a0, a1, a2, a3, pb0, pb1);
+                    mma16816(o[4 * u + 2 * lc + j], a0, a1, a2, a3, pb0, pb1);
                 }
+                if (lc == 1 || G32V)
+                    mma16816(ps[G32V ? 2 * u + lc : u], ones[0], ones[1], ones[2], ones[3], pb0, pb1);
             }
-            mma16816(ps[g], ones[0], ones[1], ones[2], ones[3], pb0, pb1);
         }
 
         }
@@ -565,7 +575,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         float *cb = reinterpret_cast<float *>(smem + C::K_OFF) + warp * (kWRows * D);
         const bool w0 = 2 * tig < R, w1 = 2 * tig + 1 < R;     // padding rows are never read
 #pragma unroll
-        for (int t = 0; t < 4 * NGV; ++t) {
+        for (int t = 0; t < 4 * NCP; ++t) {
             const int d = 32 * (t >> 1) + 4 * gid + 2 * (t & 1);
             if (w0) *reinterpret_cast<float2 *>(cb + (2 * tig) * D + d) = make_float2(o[t][0], o[t][2]);
             if (w1) *reinterpret_cast<float2 *>(cb + (2 * tig + 1) * D + d) = make_float2(o[t][1], o[t][3]);
@@ -575,7 +585,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     const int64_t rows_total = (int64_t)a.n_seq * a.n_q * a.n_heads;
     const float *cb0 = reinterpret_cast<const float *>(smem + C::K_OFF);
     for (int idx = threadIdx.x; idx < R * (D / 4); idx += C::NTH) {
-        const int r = idx / (D / 4), d = 4 * (idx % (D / 4)), g = d / 64;
+        const int r = idx / (D / 4), d = 4 * (idx % (D / 4)), g = d / C::VGS;
         // common maximum of row r and each warp's weight
         // (rolled loops: this code runs once per CTA, from a cold instruction cache)
         float M = -INFINITY;
@@ -623,16 +633,16 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int KC, int D, typename QT>
+template <int KC, int VC, int D, typename QT>
 cudaError_t warp_prepare(int *per_sm)
 {
-    using C = WCfg<KC, D, QT>;
+    using C = WCfg<KC, VC, D, QT>;
     static PerDevice pd;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int n = per_device(pd, dev, []() -> int {
-        auto kern = decode_warp_kernel<KC, D, QT>;
+        auto kern = decode_warp_kernel<KC, VC, D, QT>;
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (r != cudaSuccess) return -(int)r;
         int v = 0;
@@ -645,10 +655,10 @@ cudaError_t warp_prepare(int *per_sm)
     return cudaSuccess;
 }
 
-template <int KC, int D, typename QT>
+template <int KC, int VC, int D, typename QT>
 cudaError_t warp_launch(const DecodeArgs &a, cudaStream_t st)
 {
-    using C = WCfg<KC, D, QT>;
+    using C = WCfg<KC, VC, D, QT>;
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
     // boxes of a whole stage, and of one block (a run's odd last block)
     CUtensorMap tk, tv, tk1, tv1;
@@ -656,56 +666,59 @@ cudaError_t warp_launch(const DecodeArgs &a, cudaStream_t st)
         !make_codes_map(&tk1, a.k.qs, C::KRB, rows, kBlk) || !make_codes_map(&tv1, a.v.qs, C::VRB, rows, kBlk))
         return cudaErrorInvalidValue;
     int per_sm = 0;
-    cudaError_t e = warp_prepare<KC, D, QT>(&per_sm);
+    cudaError_t e = warp_prepare<KC, VC, D, QT>(&per_sm);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_splits, a.n_kv_heads, a.n_seq);
-    return launch_pdl(decode_warp_kernel<KC, D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv, tk1, tv1);
+    return launch_pdl(decode_warp_kernel<KC, VC, D, QT>, grid, dim3(C::NTH), C::SMEM, st, a, tk, tv, tk1, tv1);
 }
 
-template <int KC, int D>
-int warp_per_sm()
+template <int KC, int VC>
+int warp_per_sm_d(int head_dim)
 {
     int n = 0;
-    if (warp_prepare<KC, D, __half>(&n) != cudaSuccess) {
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (head_dim) {
+    case 64: e = warp_prepare<KC, VC, 64, __half>(&n); break;
+    case 128: e = warp_prepare<KC, VC, 128, __half>(&n); break;
+    case 256: e = warp_prepare<KC, VC, 256, __half>(&n); break;
+    default: break;
+    }
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-template <int KC>
-int warp_per_sm_d(int head_dim)
-{
-    switch (head_dim) {
-    case 64: return warp_per_sm<KC, 64>();
-    case 128: return warp_per_sm<KC, 128>();
-    case 256: return warp_per_sm<KC, 256>();
-    default: return 0;
-    }
-}
-
-template <int KC>
+template <int KC, int VC>
 cudaError_t warp_launch_d(const DecodeArgs &a, bool f16, cudaStream_t st)
 {
     switch (a.head_dim) {
-    case 64: return f16 ? warp_launch<KC, 64, __half>(a, st) : warp_launch<KC, 64, float>(a, st);
-    case 128: return f16 ? warp_launch<KC, 128, __half>(a, st) : warp_launch<KC, 128, float>(a, st);
-    case 256: return f16 ? warp_launch<KC, 256, __half>(a, st) : warp_launch<KC, 256, float>(a, st);
+    case 64: return f16 ? warp_launch<KC, VC, 64, __half>(a, st) : warp_launch<KC, VC, 64, float>(a, st);
+    case 128: return f16 ? warp_launch<KC, VC, 128, __half>(a, st) : warp_launch<KC, VC, 128, float>(a, st);
+    case 256: return f16 ? warp_launch<KC, VC, 256, __half>(a, st) : warp_launch<KC, VC, 256, float>(a, st);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
+// Q4_G64 V with Q4_G64 or q8_0 K; Q4_G32 V with q8_0 K (the shipped q8_0 / q4_0
+// pair; with 4-bit K the eight V groups' sums of P' and the K groups' four
+// accumulator inputs would not fit the registers together).
 bool decode_warp_shape(int k_codec, int v_codec, int head_dim, int rows_per_kv_head)
 {
-    return (k_codec == KVQ_CODEC_Q4_G64 || k_codec == KVQ_CODEC_Q8_0) && v_codec == KVQ_CODEC_Q4_G64 &&
-           rows_per_kv_head >= 1 && rows_per_kv_head <= kWRows && (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    const bool pair = (v_codec == KVQ_CODEC_Q4_G64 && (k_codec == KVQ_CODEC_Q4_G64 || k_codec == KVQ_CODEC_Q8_0)) ||
+                      (v_codec == KVQ_CODEC_Q4_G32 && k_codec == KVQ_CODEC_Q8_0);
+    return pair && rows_per_kv_head >= 1 && rows_per_kv_head <= kWRows &&
+           (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
 
-int decode_warp_ctas_per_sm(int k_codec, int head_dim)
+int decode_warp_ctas_per_sm(int k_codec, int v_codec, int head_dim)
 {
-    return k_codec == KVQ_CODEC_Q8_0 ? warp_per_sm_d<KVQ_CODEC_Q8_0>(head_dim) : warp_per_sm_d<KVQ_CODEC_Q4_G64>(head_dim);
+    if (v_codec == KVQ_CODEC_Q4_G32) return warp_per_sm_d<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4_G32>(head_dim);
+    return k_codec == KVQ_CODEC_Q8_0 ? warp_per_sm_d<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4_G64>(head_dim)
+                                     : warp_per_sm_d<KVQ_CODEC_Q4_G64, KVQ_CODEC_Q4_G64>(head_dim);
 }
 
 bool decode_warp_takes(const DecodeArgs &a)
@@ -713,14 +726,15 @@ bool decode_warp_takes(const DecodeArgs &a)
     const int R = a.n_q * (a.n_heads / a.n_kv_heads);
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
     return decode_warp_shape(a.k.codec, a.v.codec, a.head_dim, R) && rows < (1LL << 31) &&
-           tensor_maps_available() && decode_warp_ctas_per_sm(a.k.codec, a.head_dim) > 0;
+           tensor_maps_available() && decode_warp_ctas_per_sm(a.k.codec, a.v.codec, a.head_dim) > 0;
 }
 
 cudaError_t launch_decode_warp(const DecodeArgs &a, int q_dtype, cudaStream_t st)
 {
     const bool f16 = q_dtype == KVQ_F16;
-    return a.k.codec == KVQ_CODEC_Q8_0 ? warp_launch_d<KVQ_CODEC_Q8_0>(a, f16, st)
-                                       : warp_launch_d<KVQ_CODEC_Q4_G64>(a, f16, st);
+    if (a.v.codec == KVQ_CODEC_Q4_G32) return warp_launch_d<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4_G32>(a, f16, st);
+    return a.k.codec == KVQ_CODEC_Q8_0 ? warp_launch_d<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4_G64>(a, f16, st)
+                                       : warp_launch_d<KVQ_CODEC_Q4_G64, KVQ_CODEC_Q4_G64>(a, f16, st);
 }
 
 }  // namespace kvq

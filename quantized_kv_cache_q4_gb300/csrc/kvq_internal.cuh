@@ -205,7 +205,7 @@ int decode_tc_fp4v_ctas_per_sm(int k_codec, int head_dim, int n_tiles);
 // decode_warp_takes: it runs these arguments.
 bool decode_warp_shape(int k_codec, int v_codec, int head_dim, int rows_per_kv_head);
 bool decode_warp_takes(const DecodeArgs &a);
-int decode_warp_ctas_per_sm(int k_codec, int head_dim);
+int decode_warp_ctas_per_sm(int k_codec, int v_codec, int head_dim);
 cudaError_t launch_decode_warp(const DecodeArgs &a, int q_dtype, cudaStream_t st);
 // Prompt-chunk path on the fifth-generation tensor cores (tcgen05): blocks of
 // 128 query rows per CTA, Q4_G64 K and V, head_dim 64/128/256,
