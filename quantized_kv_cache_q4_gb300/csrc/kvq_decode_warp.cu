@@ -226,11 +226,15 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     int lo, hi;
     split_range(len, a.n_splits, split, lo, hi);
     // this warp's blocks: a contiguous run [wb0, wb0 + my_nb) of the split's
-    // 16-token blocks, streamed kSBlk to a ring stage
+    // 16-token blocks.  The run's first ring stage holds one block, every later
+    // one kSBlk (the last the remainder): the whole grid issues its first
+    // copies at once, and a smaller first copy lands sooner, so the warps start
+    // computing while the rest of that wave is still arriving.
     const int nb = (int)ceil_div(hi - lo, kBlk);
     const int wb0 = (warp * nb) / kWW;
     const int my_nb = ((warp + 1) * nb) / kWW - wb0;
-    const int n_st = (my_nb + kSBlk - 1) / kSBlk;
+    const int n_st = my_nb > 0 ? 1 + (my_nb + kSBlk - 2) / kSBlk : 0;
+    auto stage_blocks = [&](int j) { return j == 0 ? 1 : min(kSBlk, my_nb - 1 - kSBlk * (j - 1)); };
     const int64_t plane_row = ((int64_t)s * a.n_kv_heads + kh) * a.capacity;
     const uint8_t *ksc = reinterpret_cast<const uint8_t *>(a.k.sc);
     const uint8_t *vsc = reinterpret_cast<const uint8_t *>(a.v.sc);
@@ -244,14 +248,14 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
     // lane 0 fills (and refills) the warp's stages in order; the cache is read
     // once per call, so evict-first in L2.  A stage's codes are one box of
     // kSBlk * 16 rows per plane (two side by side for 256-byte K rows), a box
-    // of 16 rows (maps tmk1, tmv1) for a run's odd last block; the scales are
+    // of 16 rows (maps tmk1, tmv1) for a stage of one block; the scales are
     // copied for the blocks the stage holds.
     int n_issued = 0, iss_slot = 0;
     int iss_row = (int)(plane_row + lo) + kBlk * wb0;      // the next stage's first plane row
     const uint64_t pol = evict_first_policy();
     auto issue = [&]() {
         const uint32_t bar = bar_ring + 8 * (uint32_t)iss_slot;
-        const uint32_t nbl = (uint32_t)min(kSBlk, my_nb - kSBlk * n_issued);
+        const uint32_t nbl = (uint32_t)stage_blocks(n_issued);
         const bool full = (nbl == (uint32_t)kSBlk);
         const CUtensorMap *mk = full ? &tmk : &tmk1, *mv = full ? &tmv : &tmv1;
         mbar_expect_tx(bar, nbl * (uint32_t)(kBlk * (C::KRB + C::VRB) + C::SBKB + C::SBVB));
@@ -265,7 +269,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
         bulk_load_hint(vs_ring + (uint32_t)iss_slot * C::SBV, vsc + (int64_t)iss_row * (NGV * 2), nbl * C::SBVB, bar,
                        pol);
         ++n_issued;
-        iss_row += kBlk * kSBlk;
+        iss_row += kBlk * (int)nbl;
         iss_slot = (iss_slot + 1 == kWS) ? 0 : iss_slot + 1;
     };
     // each warp's first stage now, its second after the query preparation (an
@@ -362,7 +366,7 @@ decode_warp_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk, 
                 stuck = j;
             }
         }
-        const int nbl = min(kSBlk, my_nb - kSBlk * j);
+        const int nbl = stage_blocks(j);
 #pragma unroll 1
         for (int b = 0; b < nbl; ++b, t0 += kBlk) {
         const uint32_t kb_addr = k_ring + (uint32_t)slot * C::CBK + (uint32_t)(b * kBlk * C::KBI) + k_off0;
@@ -660,7 +664,8 @@ cudaError_t warp_launch(const DecodeArgs &a, cudaStream_t st)
 {
     using C = WCfg<KC, VC, D, QT>;
     const int64_t rows = (int64_t)a.n_seq * a.n_kv_heads * a.capacity;
-    // boxes of a whole stage, and of one block (a run's odd last block)
+    // boxes of a whole stage, and of one block (a run's first stage, and its
+    // last where the rest of the run is odd)
     CUtensorMap tk, tv, tk1, tv1;
     if (!make_codes_map(&tk, a.k.qs, C::KRB, rows, C::ST) || !make_codes_map(&tv, a.v.qs, C::VRB, rows, C::ST) ||
         !make_codes_map(&tk1, a.k.qs, C::KRB, rows, kBlk) || !make_codes_map(&tv1, a.v.qs, C::VRB, rows, kBlk))
