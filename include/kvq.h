@@ -43,7 +43,7 @@ extern "C" {
 typedef enum kvq_status {
     KVQ_OK = 0,
     KVQ_EINVAL = 1,        /* a null pointer, a bad size or an inconsistent shape */
-    KVQ_EUNSUPPORTED = 2,  /* a valid request this build does not implement */
+    KVQ_EUNSUPPORTED = 2,  /* a valid request the library does not implement */
     KVQ_EWORKSPACE = 3,    /* workspace missing or smaller than kvq_decode_workspace_bytes() */
     KVQ_ECUDA = 4          /* a CUDA call or kernel launch failed */
 } kvq_status;
