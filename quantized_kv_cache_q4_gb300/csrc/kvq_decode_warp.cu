@@ -1,17 +1,19 @@
 // kvq_decode_warp.cu -- split-K decode attention for up to 8 query rows per
 // kv head (a GQA group of one token, or 1 + k MTP tokens of a narrow group)
-// over a Q4_G64 V plane and a Q4_G64 or q8_0 K plane: one CTA of 12 warps per
-// SM, each warp owning whole blocks of 16 tokens over all of head_dim.
-// (den_llama.cpp, "What's in the fork": the fattn-vec Q4_G64 instances; "What
-// this fork is": 4-bit signed codes sharing one fp16 scale per 64 values, and
-// the q8_0 K / Q4_G64 V pair.)
+// over a Q4_G64 V plane with a Q4_G64 or q8_0 K plane, or the q8_0 K / Q4_G32 V
+// pair: one CTA of 12 warps per SM, each warp owning whole blocks of 16 tokens
+// over all of head_dim.  (den_llama.cpp, "What's in the fork": the fattn-vec
+// Q4_G64 instances; "What this fork is": 4-bit signed codes sharing one fp16
+// scale per 64 values, the q8_0 K / Q4_G64 V pair, and the q8_0 K / q4_0 V
+// FlashAttention pair, q4_0 read as 4-bit codes with a scale per 32 values.)
 //
 // Per (sequence, kv head, split) the split's tokens are cut into blocks of 16
 // and each warp takes a contiguous run of them, streamed through its own ring
 // of two shared-memory stages (K and V codes by 2D TMA, 32 rows a box for
-// 4-bit K, 16 for q8_0 K, whose rows take two 128-byte boxes; the fp16 scales
-// by bulk copies).  Each warp keeps its own online-softmax state, so nothing
-// in the loop waits on another warp.  Per block the warp:
+// 4-bit K after a first stage of 16, 16 for q8_0 K, whose rows take two
+// 128-byte boxes; the fp16 scales by bulk copies).  Each warp keeps its own
+// online-softmax state, so nothing in the loop waits on another warp.  Per
+// block the warp:
 //  * computes S^T = K Q^T (tokens on M, query rows on N) on mma.sync.m16n8k16:
 //    the K codes enter as exact fp16 integers with their bias (4-bit: 1032 + q,
 //    or 1152 + 16 q at odd head_dim indices, one LOP3 per two values; q8_0:
